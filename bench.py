@@ -1,0 +1,415 @@
+"""Benchmark: GFLOP/s and fraction of the FP32 CUDA-core roofline.
+
+Headline (``value``): the exact-mode fp32 product C = A*B at m = n = k = 4096
+(A, B ~ N(0, 1), row-major, contiguous), one om_gemm_f32 call per step,
+inputs resident in HBM, L2 flushed (a 512 MiB write) before every timed
+call. Also reported per step set: fast mode on the same product, the
+ResNet-50 stage-1 3x3 and 1x1 convolutions (exact and fast), the prefill
+product and the grouped/strided/dilated convolution.
+
+Roofline: the kernels are bound by the FP32 pipes (bound "alu"). The peak is
+derived from unit counts and the maximum SM clock: SMs x 128 FP32 lanes x 2
+flops x 2070 MHz (fast mode, one fused multiply-add per term); exact mode
+issues a multiply and an add per term, so its ceiling is half of that.
+
+``--impl reference`` times the CPU oracle (plain C loops of the definition)
+on the host cores on a bounded row sample of the same product.
+
+Multi-GPU (torchrun, N > 1): every rank runs its own replica of the workload
+on its own GPU; there is no data exchange. value = work of all ranks / the
+slowest rank's time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SM_MAX_MHZ = 2070.0
+FP32_LANES_PER_SM = 128
+
+
+def fp32_peak_tflops(sms: int, exact: bool) -> float:
+    p = sms * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    return p / 2 if exact else p
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- workloads
+def gemm_workload():
+    from implicit_gemm_convolution_gb300 import synth
+    return synth.workload_gemm_4096()
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "implicit_gemm_convolution_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    e = rec.get(f"{kernel}:{workload}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class L2Flusher:
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_calls(fn, steps: int, warmup: int, flush, stream) -> list[float]:
+    """Per-call device time (ms) of fn on stream, L2 flushed before each call."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import implicit_gemm_convolution_gb300 as om
+    from implicit_gemm_convolution_gb300 import synth
+
+    om.build()
+    om.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flush = L2Flusher(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+
+    case = gemm_workload()
+    m, n, k = case.m, case.n, case.k
+    flops = 2.0 * m * n * k
+    A = torch.from_numpy(case.A).to(dev)
+    B = torch.from_numpy(case.B).to(dev)
+    C = torch.empty((m, n), dtype=torch.float32, device=dev)
+
+    def step_exact():
+        st = om.gemm_raw(m, n, k, A.data_ptr(), k, B.data_ptr(), n, C.data_ptr(), n, "exact", stream)
+        if st != 0:
+            raise RuntimeError(f"om_gemm_f32 failed: {om.STATUS_NAMES.get(st, st)}")
+
+    # ---- headline: K timed steps bracketed by barrier + synchronize
+    for _ in range(args.warmup):
+        flush()
+        step_exact()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        t_wall0 = time.perf_counter()
+        kernel_ms = []
+        for _ in range(args.steps):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step_exact()
+            e1.record(stream)
+            e1.synchronize()
+            kernel_ms.append(e0.elapsed_time(e1))
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    ms_local = float(np.mean(kernel_ms))
+    ms = ms_local
+    if dist is not None:
+        t = torch.tensor([ms_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    value = world * flops / (ms * 1e-3) / 1e9  # GFLOP/s over all ranks
+    achieved_tflops = flops / (ms_local * 1e-3) / 1e12
+    peak_exact = fp32_peak_tflops(sms, exact=True)
+
+    if rank != 0:
+        return None
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    hA = torch.from_numpy(case.A).pin_memory()
+    hB = torch.from_numpy(case.B).pin_memory()
+    hC = torch.empty((m, n), dtype=torch.float32).pin_memory()
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        st = om.gemm_raw(m, n, k, dA.data_ptr(), k, dB.data_ptr(), n, C.data_ptr(), n, "exact",
+                         stream)
+        if st != 0:
+            raise RuntimeError("om_gemm_f32 failed")
+        hC.copy_(C, non_blocking=True)
+
+    e2e_ms = float(np.mean(time_calls(e2e_step, max(2, args.steps // 2), 2, flush, stream)))
+    e2e = {"value": round(flops / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
+           "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
+           "d2h_bytes_per_step": int(hC.numel() * 4), "ms_per_step": round(e2e_ms, 4)}
+
+    # ---- per-mode and per-workload lines (same timing rules)
+    extras = {}
+
+    def gemm_line(name, mode, case_):
+        Ad = torch.from_numpy(case_.A).to(dev)
+        Bd = torch.from_numpy(case_.B).to(dev)
+        Cd = torch.from_numpy(case_.C_init).to(dev)
+
+        def f():
+            st = om.gemm_raw(case_.m, case_.n, case_.k, Ad.data_ptr(), case_.lda, Bd.data_ptr(),
+                             case_.ldb, Cd.data_ptr(), case_.ldc, mode, stream)
+            if st != 0:
+                raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
+        t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
+        fl = 2.0 * case_.m * case_.n * case_.k
+        tf = fl / (t * 1e-3) / 1e12
+        pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
+        extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
+                        "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
+
+    def conv_line(name, mode, c):
+        x = torch.from_numpy(c.x).to(dev)
+        w = torch.from_numpy(c.w).to(dev)
+        OH = om.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.dil)
+        OW = om.conv_out_dim(c.W, c.KW, c.stride, c.pad, c.dil)
+        y = torch.empty((c.N, c.Cout, OH, OW), dtype=torch.float32, device=dev)
+        L = om.lib()
+
+        def f():
+            st = L.om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad,
+                                 c.dil, x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[mode],
+                                 stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
+        t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
+        fl = 2.0 * c.N * c.Cout * OH * OW * (c.Cin // c.G) * c.KH * c.KW
+        tf = fl / (t * 1e-3) / 1e12
+        pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
+        extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
+                        "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
+
+    if not args.headline_only:
+        gemm_line("gemm_4096^3_fast", "fast", case)
+        gemm_line("gemm_prefill_512x11008x4096_exact", "exact", synth.workload_gemm_prefill(False))
+        gemm_line("gemm_prefill_509x11005x4096_exact", "exact", synth.workload_gemm_prefill(True))
+        for md in ("exact", "fast"):
+            conv_line(f"conv3x3_n32_c64_56_{md}", md, synth.workload_conv3x3())
+            conv_line(f"conv1x1_n32_c256to64_56_{md}", md, synth.workload_conv1x1())
+        conv_line("conv_g32_s2_d2_n16_c256_28_exact", "exact", synth.workload_conv_grouped())
+
+    cpu = cpu_baseline(args.cpu_seconds)
+    line = {
+        "metric": "GFLOP/s and % of FP32 CUDA-core roofline per mode (GEMM 4096^3; conv3x3)",
+        "value": round(value, 1),
+        "unit": "GFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64, N(0,1) operands)",
+        "config": {"workload": "gemm_4096^3", "m": m, "n": n, "k": k, "mode": "exact",
+                   "layout": "row-major contiguous", "l2": "flushed before every timed call",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "alu", "achieved": round(achieved_tflops, 3),
+                     "peak": round(peak_exact, 3), "unit": "TFLOP/s",
+                     "frac": round(achieved_tflops / peak_exact, 4),
+                     "traffic": recorded_traffic("sgemm_tiled_kernel", "gemm_4096^3_exact"),
+                     "peak_basis": f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x {SM_MAX_MHZ:.0f} MHz / 2 "
+                                   "(exact mode issues a multiply and an add per term)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+        "modes": extras,
+    }
+    return line
+
+
+def cpu_baseline(seconds: float) -> dict:
+    """The oracle as it stands on the host cores: exact mode on a growing
+    sample of whole rows of the 4096-cube product until ~seconds of work."""
+    import oracle
+    case = gemm_workload()
+    threads = oracle.default_threads()
+    rows = threads
+    elapsed = 0.0
+    while True:
+        Cs = np.zeros((rows, case.n), np.float32)
+        t0 = time.perf_counter()
+        oracle.gemm_raw(rows, case.n, case.k, case.A[:rows].copy(), case.k, case.B, case.n, Cs,
+                        case.n, oracle.EXACT, threads)
+        elapsed = time.perf_counter() - t0
+        if elapsed >= seconds / 4 or rows >= case.m:
+            break
+        rows = min(case.m, rows * 4)
+    gflops = 2.0 * rows * case.n * case.k / elapsed / 1e9
+    return {"value": round(gflops, 3), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"exact mode, first {rows} of 4096 rows of the 4096^3 product "
+                      f"({elapsed:.2f} s, OpenMP over rows)"}
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    case = gemm_workload()
+    threads = oracle.default_threads()
+    rows = max(threads, 16)
+    A = case.A[:rows].copy()
+    Cs = np.zeros((rows, case.n), np.float32)
+
+    def step():
+        oracle.gemm_raw(rows, case.n, case.k, A, case.k, case.B, case.n, Cs, case.n, oracle.EXACT,
+                        threads)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    val = 2.0 * rows * case.n * case.k / dt / 1e9
+    sample = f"exact mode, {rows} of 4096 rows of the 4096^3 product per step"
+    return {"impl": "reference", "metric": "GFLOP/s and % of FP32 CUDA-core roofline per mode (GEMM 4096^3; conv3x3)",
+            "value": round(val, 3), "unit": "GFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64, N(0,1) operands)",
+            "config": {"workload": "gemm_4096^3", "m": 4096, "n": 4096, "k": 4096, "mode": "exact"},
+            "cpu_baseline": {"value": round(val, 3), "unit": "GFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--extra-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--headline-only", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

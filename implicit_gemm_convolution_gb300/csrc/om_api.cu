@@ -1,0 +1,257 @@
+// om_api.cu -- the C ABI declared in include/om.h: argument validation, shape
+// derivation, kernel selection and launch on the caller's stream.
+//
+// The library allocates no device memory and keeps no state between calls
+// besides a per-device cache of the SM count.
+#include <cstdint>
+#include <cstdlib>
+
+#include "om.h"
+#include "om_internal.h"
+
+namespace om {
+
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int v = 1;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) v = 1;
+    if (dev < 64) cached[dev] = v;
+    return v;
+}
+
+}  // namespace om
+
+namespace {
+
+using om::ConvProblem;
+using om::GemmProblem;
+
+// A test-only override of the kernel configuration; every configuration
+// computes the same bits.
+int forced(const char *name) {
+    const char *v = std::getenv(name);
+    if (!v || !*v) return -1;
+    return std::atoi(v);
+}
+
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
+// Byte range [lo, hi) touched by a row-major rows x cols block with row stride ld.
+struct Range {
+    uintptr_t lo, hi;
+};
+
+bool block_range(const void *base, int64_t rows, int64_t cols, int64_t ld, Range *r) {
+    r->lo = r->hi = reinterpret_cast<uintptr_t>(base);
+    if (rows <= 0 || cols <= 0) return true;
+    const __int128 elems = static_cast<__int128>(rows - 1) * ld + cols;
+    if (elems >= (static_cast<__int128>(1) << 60)) return false;
+    r->hi = r->lo + static_cast<uintptr_t>(elems) * 4;
+    return r->hi > r->lo;
+}
+
+Range span(const void *base, __int128 elems) {
+    Range r;
+    r.lo = reinterpret_cast<uintptr_t>(base);
+    r.hi = r.lo + static_cast<uintptr_t>(elems) * 4;
+    return r;
+}
+
+bool overlaps(const Range &a, const Range &b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? OM_OK : OM_ERR_CUDA; }
+
+int64_t out_dim(int64_t size, int64_t k, int64_t stride, int64_t pad, int64_t dil) {
+    const int64_t num = size + 2 * pad - dil * (k - 1) - 1;
+    if (num < 0) return 0;
+    return num / stride + 1;
+}
+
+struct ConvArgs {
+    int64_t N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil;
+};
+
+// Validates a convolution call and fills the problem; returns an om_status.
+int validate_conv(const ConvArgs &a, const float *x, const float *w, bool packed, float *y,
+                  int mode, ConvProblem *p, bool *empty) {
+    *empty = false;
+    if (a.N < 0 || a.Cin < 0 || a.H < 0 || a.W < 0 || a.Cout < 0) return OM_ERR_INVALID_ARG;
+    if (a.G < 1 || a.KH < 1 || a.KW < 1 || a.stride < 1 || a.dil < 1 || a.pad < 0)
+        return OM_ERR_INVALID_ARG;
+    if (a.Cin % a.G != 0 || a.Cout % a.G != 0) return OM_ERR_INVALID_ARG;
+    if (mode != OM_MODE_EXACT && mode != OM_MODE_FAST) return OM_ERR_UNSUPPORTED;
+    // Size bounds keep every derived quantity inside int64 and the kernels'
+    // 32-bit per-image indices from overflowing.
+    const int64_t lim31 = (int64_t(1) << 31) - 1;
+    if (a.H > lim31 || a.W > lim31 || a.KH > 65535 || a.KW > 65535 || a.stride > 65535 ||
+        a.dil > 65535 || a.pad > 65535)
+        return OM_ERR_TOO_LARGE;
+    const int64_t OH = out_dim(a.H, a.KH, a.stride, a.pad, a.dil);
+    const int64_t OW = out_dim(a.W, a.KW, a.stride, a.pad, a.dil);
+    const int64_t cin_g = a.Cin / a.G;
+    const __int128 K = static_cast<__int128>(cin_g) * a.KH * a.KW;
+    const __int128 Kp = (K + 3) / 4 * 4;
+    const __int128 w_ld = packed ? Kp : K;
+    const __int128 xe = static_cast<__int128>(a.N) * a.Cin * a.H * a.W;
+    const __int128 ye = static_cast<__int128>(a.N) * a.Cout * OH * OW;
+    const __int128 we = static_cast<__int128>(a.Cout) * w_ld;
+    const __int128 lim62 = static_cast<__int128>(1) << 62;
+    if (K > lim31 || xe >= lim62 || ye >= lim62 || we >= lim62) return OM_ERR_TOO_LARGE;
+    if (static_cast<__int128>(a.Cin) * a.H * a.W > lim31 ||
+        static_cast<__int128>(a.Cout) * OH * OW > lim31)
+        return OM_ERR_TOO_LARGE;
+    if (ye == 0) {
+        *empty = true;
+        return OM_OK;
+    }
+    if (!y) return OM_ERR_NULL_PTR;
+    if (xe > 0 && !x) return OM_ERR_NULL_PTR;
+    if (K > 0 && !w) return OM_ERR_NULL_PTR;
+    if (!aligned4(x) || !aligned4(w) || !aligned4(y)) return OM_ERR_ALIGNMENT;
+    if (packed && (reinterpret_cast<uintptr_t>(w) & 15) != 0) return OM_ERR_ALIGNMENT;
+    const Range ry = span(y, ye), rx = span(x, xe), rw = span(w, we);
+    if ((xe > 0 && overlaps(ry, rx)) || (K > 0 && overlaps(ry, rw))) return OM_ERR_ALIAS;
+    p->N = a.N; p->Cin = a.Cin; p->H = a.H; p->W = a.W; p->Cout = a.Cout; p->G = a.G;
+    p->KH = a.KH; p->KW = a.KW;
+    p->sH = p->sW = a.stride;
+    p->pT = p->pL = a.pad;
+    p->dH = p->dW = a.dil;
+    p->OH = OH; p->OW = OW;
+    p->K = static_cast<int64_t>(K);
+    p->w_ld = static_cast<int64_t>(w_ld);
+    p->x = x; p->w = w; p->y = y;
+    return OM_OK;
+}
+
+int run_conv(const ConvProblem &p, int mode, cudaStream_t s) {
+    int cfg = forced("OM_FORCE_CONV_CFG");
+    if (cfg == om::kConvNaive || p.K == 0) return from_cuda(om::launch_conv_naive(p, mode, s));
+    cudaError_t e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, s);
+    if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int om_version(void) { return OM_VERSION; }
+
+const char *om_status_string(int status) {
+    switch (status) {
+        case OM_OK: return "OM_OK";
+        case OM_ERR_INVALID_ARG: return "OM_ERR_INVALID_ARG";
+        case OM_ERR_NULL_PTR: return "OM_ERR_NULL_PTR";
+        case OM_ERR_ALIAS: return "OM_ERR_ALIAS";
+        case OM_ERR_UNSUPPORTED: return "OM_ERR_UNSUPPORTED";
+        case OM_ERR_CUDA: return "OM_ERR_CUDA";
+        case OM_ERR_TIMEOUT: return "OM_ERR_TIMEOUT";
+        case OM_ERR_ALIGNMENT: return "OM_ERR_ALIGNMENT";
+        case OM_ERR_TOO_LARGE: return "OM_ERR_TOO_LARGE";
+        default: return "OM_UNKNOWN";
+    }
+}
+
+int64_t om_conv_out_dim(int64_t size, int64_t ksize, int64_t stride, int64_t pad, int64_t dil) {
+    if (size < 0 || ksize < 1 || stride < 1 || pad < 0 || dil < 1) return -1;
+    if (size > (int64_t(1) << 40) || ksize > (int64_t(1) << 20) || pad > (int64_t(1) << 40) ||
+        dil > (int64_t(1) << 20) || stride > (int64_t(1) << 40))
+        return -1;
+    return out_dim(size, ksize, stride, pad, dil);
+}
+
+int om_gemm_f32(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, const float *B,
+                int64_t ldb, float *C, int64_t ldc, int mode, void *stream) {
+    if (m < 0 || n < 0 || k < 0) return OM_ERR_INVALID_ARG;
+    if (mode != OM_MODE_EXACT && mode != OM_MODE_FAST && mode != OM_MODE_TF32X3)
+        return OM_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0) return OM_OK;
+    const bool used = k > 0;
+    if (used && (lda < k || ldb < n)) return OM_ERR_INVALID_ARG;
+    if (ldc < n) return OM_ERR_INVALID_ARG;
+    if (!C || (used && (!A || !B))) return OM_ERR_NULL_PTR;
+    if (!aligned4(C) || (used && (!aligned4(A) || !aligned4(B)))) return OM_ERR_ALIGNMENT;
+    Range rc, ra, rb;
+    if (!block_range(C, m, n, ldc, &rc)) return OM_ERR_TOO_LARGE;
+    if (used && !block_range(A, m, k, lda, &ra)) return OM_ERR_TOO_LARGE;
+    if (used && !block_range(B, k, n, ldb, &rb)) return OM_ERR_TOO_LARGE;
+    if (used && (overlaps(rc, ra) || overlaps(rc, rb))) return OM_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc};
+    if (mode == OM_MODE_TF32X3) return OM_ERR_UNSUPPORTED;
+    const int cfg = forced("OM_FORCE_GEMM_CFG");
+    if (k == 0 || cfg == om::kCfgNaive) return from_cuda(om::launch_gemm_naive(p, mode, s));
+    cudaError_t e;
+    if (cfg > 0) {
+        e = om::launch_gemm_tiled(p, mode, cfg, s);
+    } else {
+        e = om::launch_gemm_tiled(p, mode, om::kCfgTma128x256, s);
+        if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, mode, om::kCfgAsync128x128, s);
+    }
+    if (e == cudaErrorNotSupported) e = om::launch_gemm_naive(p, mode, s);
+    return from_cuda(e);
+}
+
+int om_conv2d_f32(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout, int64_t G,
+                  int64_t KH, int64_t KW, int64_t stride, int64_t pad, int64_t dil,
+                  const float *x, const float *w, float *y, int mode, void *stream) {
+    const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
+    ConvProblem p;
+    bool empty = false;
+    const int st = validate_conv(a, x, w, false, y, mode, &p, &empty);
+    if (st != OM_OK || empty) return st;
+    return run_conv(p, mode, static_cast<cudaStream_t>(stream));
+}
+
+int om_pack_conv_weights(int64_t Cout, int64_t Cin, int64_t G, int64_t KH, int64_t KW,
+                         const float *w, float *w_packed, size_t *packed_bytes, void *stream) {
+    if (Cout < 0 || Cin < 0 || G < 1 || KH < 1 || KW < 1) return OM_ERR_INVALID_ARG;
+    if (Cin % G != 0 || Cout % G != 0) return OM_ERR_INVALID_ARG;
+    if (KH > 65535 || KW > 65535) return OM_ERR_TOO_LARGE;
+    const __int128 K = static_cast<__int128>(Cin / G) * KH * KW;
+    if (K > (int64_t(1) << 31) - 1) return OM_ERR_TOO_LARGE;
+    const int64_t Kp = (static_cast<int64_t>(K) + 3) / 4 * 4;
+    const __int128 bytes = static_cast<__int128>(Cout) * Kp * 4;
+    if (bytes >= (static_cast<__int128>(1) << 62)) return OM_ERR_TOO_LARGE;
+    if (!w_packed) {
+        if (!packed_bytes) return OM_ERR_NULL_PTR;
+        *packed_bytes = static_cast<size_t>(bytes);
+        return OM_OK;
+    }
+    if (packed_bytes) *packed_bytes = static_cast<size_t>(bytes);
+    if (bytes == 0) return OM_OK;
+    if (K > 0 && !w) return OM_ERR_NULL_PTR;
+    if ((reinterpret_cast<uintptr_t>(w_packed) & 15) != 0 || !aligned4(w)) return OM_ERR_ALIGNMENT;
+    const Range rp = span(w_packed, bytes / 4), rw = span(w, static_cast<__int128>(Cout) * K);
+    if (K > 0 && overlaps(rp, rw)) return OM_ERR_ALIAS;
+    return from_cuda(om::launch_pack_conv_weights(Cout, static_cast<int64_t>(K), Kp, w, w_packed,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+int om_conv2d_f32_packed(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout, int64_t G,
+                         int64_t KH, int64_t KW, int64_t stride, int64_t pad, int64_t dil,
+                         const float *x, const float *w_packed, float *y, int mode,
+                         void *stream) {
+    const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
+    ConvProblem p;
+    bool empty = false;
+    const int st = validate_conv(a, x, w_packed, true, y, mode, &p, &empty);
+    if (st != OM_OK || empty) return st;
+    return run_conv(p, mode, static_cast<cudaStream_t>(stream));
+}
+
+int om_device_status(void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned a = 0, b = 0;
+    if (om::read_clear_status_gemm(&a, s) != cudaSuccess) return OM_ERR_CUDA;
+    if (om::read_clear_status_conv(&b, s) != cudaSuccess) return OM_ERR_CUDA;
+    return ((a | b) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,151 @@
+// om_device.cuh -- device-side building blocks shared by the library's kernels:
+// the per-term arithmetic of the two bit-exact modes, the canonical-NaN store,
+// mbarrier / TMA / cp.async wrappers in inline PTX, and bounded waits.
+//
+// Arithmetic follows the OneModel "Exact mode" page (rules 1-4 and section
+// "Matrix product"): exact mode is round(acc + round(a*b)) with the multiply
+// and the add rounded separately; fast mode ("Matrix product and convolution
+// kernels" page, section "Fast mode") is one fused multiply-add per term.
+// The library is compiled with -fmad=false and without -ftz, and uses the
+// explicitly rounded _rn intrinsics, which the compiler never contracts.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace om {
+
+enum Mode : int { kExact = 0, kFast = 1 };
+
+// Bit of a translation unit's device status word set by a bounded wait that
+// ran out; om_device_status() reads and clears the words.
+constexpr unsigned kDevErrTimeout = 1u;
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+
+__device__ __forceinline__ float canonical_nan(float v) {
+    // Every stored NaN becomes the quiet NaN 0x7FC00000.
+    return (v != v) ? __int_as_float(0x7FC00000) : v;
+}
+
+template <int MODE>
+__device__ __forceinline__ float term(float acc, float a, float b) {
+    if constexpr (MODE == kFast) {
+        return __fmaf_rn(a, b, acc);
+    } else {
+        return __fadd_rn(acc, __fmul_rn(a, b));
+    }
+}
+
+// Two independent outputs at once (paired-lane fp32 instructions of sm_100+).
+// Each lane is rounded on its own exactly like the scalar form above.
+template <int MODE>
+__device__ __forceinline__ float2 term2(float2 acc, float2 a, float2 b) {
+    if constexpr (MODE == kFast) {
+        return __ffma2_rn(a, b, acc);
+    } else {
+        return __fadd2_rn(acc, __fmul2_rn(a, b));
+    }
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after the
+// time limit (the caller records the error and leaves).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// ---------------------------------------------------------------- cp.async
+// 4-byte copy global -> shared; src_bytes == 0 writes +0 without reading.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on bar once every cp.async this thread issued so far has landed.
+// The barrier's expected count must include this arrival (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+}  // namespace om

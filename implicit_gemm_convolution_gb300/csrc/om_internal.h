@@ -1,0 +1,73 @@
+// om_internal.h -- host-side interface between the C ABI (om_api.cu) and the
+// kernel translation units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace om {
+
+// A validated row-major product problem (device pointers).
+struct GemmProblem {
+    int64_t m, n, k;
+    const float *A;
+    int64_t lda;
+    const float *B;
+    int64_t ldb;
+    float *C;
+    int64_t ldc;
+};
+
+// A validated convolution problem. Weights are read as the matrix
+// w[oc][p] with row stride w_ld (K for the caller's layout, Kp for the
+// packed layout), p = (c*KH + ky)*KW + kx.
+struct ConvProblem {
+    int64_t N, Cin, H, W, Cout, G, KH, KW;
+    int64_t sH, sW, pT, pL, dH, dW;
+    int64_t OH, OW;
+    int64_t K;     // Cin/G*KH*KW
+    int64_t w_ld;  // row stride of the weight matrix (>= K)
+    const float *x;
+    const float *w;
+    float *y;
+};
+
+// Kernel configurations the dispatcher can choose. A test-only environment
+// override (OM_FORCE_GEMM_CFG / OM_FORCE_CONV_CFG) forces one; every
+// configuration gives identical bits.
+enum GemmCfg : int {
+    kCfgAuto = -1,
+    kCfgNaive = 0,             // one thread per output
+    kCfgTma128x256 = 1,        // TMA-fed SIMT tiles, 128x256, paired-lane fp32
+    kCfgTma128x128 = 2,        // TMA-fed SIMT tiles, 128x128, paired-lane fp32
+    kCfgAsync128x128 = 3,      // 4-byte cp.async-fed SIMT tiles (any alignment)
+    kCfgTmaScalar128x256 = 4,  // as 1 with one-lane fp32 instructions
+};
+
+enum ConvCfg : int {
+    kConvAuto = -1,
+    kConvNaive = 0,     // one thread per output, direct loops
+    kConvImplicit = 1,  // implicit GEMM with gathered patches
+};
+
+cudaError_t launch_gemm_naive(const GemmProblem &p, int mode, cudaStream_t s);
+cudaError_t launch_conv_naive(const ConvProblem &p, int mode, cudaStream_t s);
+cudaError_t launch_pack_conv_weights(int64_t Cout, int64_t K, int64_t Kp, const float *w,
+                                     float *w_packed, cudaStream_t s);
+
+// Tiled kernels. Return cudaErrorNotSupported when the configuration cannot
+// run this problem (the dispatcher then picks another one).
+cudaError_t launch_gemm_tiled(const GemmProblem &p, int mode, int cfg, cudaStream_t s);
+cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, cudaStream_t s);
+
+// Read and clear the device status word of the tiled translation units
+// (synchronises s).
+cudaError_t read_clear_status_gemm(unsigned *out, cudaStream_t s);
+cudaError_t read_clear_status_conv(unsigned *out, cudaStream_t s);
+
+int num_sms();
+
+// Bit of the device status words set by a bounded wait that ran out.
+constexpr unsigned kDevErrTimeoutHost = 1u;
+
+}  // namespace om

@@ -1,0 +1,155 @@
+// simt_tile.cuh -- the shared-memory tile layout and the register-tile inner
+// loop used by the tiled matrix product and the implicit-GEMM convolution.
+//
+// Per output the loop adds one term per k in increasing k, from the
+// accumulator the previous stage left ("Exact mode" page, section "Matrix
+// product"; the k-block continuation of the "Matrix product and convolution
+// kernels" page, item 3 "Microkernel"). The accumulators stay in registers
+// for the whole of k, so a stage boundary adds no rounding.
+//
+// Shared-memory stage: A tile BM x 32 (k innermost), 128-byte swizzled: row r,
+// 16-byte chunk c is stored at chunk c ^ (r % 8) of the row's 128 bytes (the
+// pattern TMA's 128B swizzle writes). B tile 32 x BN, row-major. Thread
+// (ty, tx) of a warp owns rows arow0 + 8i (i < TM) and columns
+// bcol0 + 16q + e (q < TN/4, e < 4) of its warp tile. One 128-bit load gives
+// four consecutive k of one A row (the swizzle keeps the eight rows of a
+// load instruction on distinct banks) or four consecutive B columns.
+#pragma once
+
+#include "om_device.cuh"
+
+namespace om {
+
+template <int BM_, int BN_, int TM_, int TN_, int WARPS_M_, int WARPS_N_, int STAGES_, bool X2_>
+struct TileCfg {
+    static constexpr int BM = BM_, BN = BN_, BK = 32, TM = TM_, TN = TN_;
+    static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
+    static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
+    static constexpr int CONSUMERS = CONSUMER_WARPS * 32;
+    static constexpr int STAGES = STAGES_;
+    static constexpr bool X2 = X2_;
+    static constexpr int WM = BM / WARPS_M, WN = BN / WARPS_N;
+    static_assert(WM == 8 * TM, "a warp tile is 8 thread rows of TM rows");
+    static_assert(WN == 4 * TN, "a warp tile is 4 thread columns of TN columns");
+    static_assert(TN % 4 == 0, "columns come in groups of four");
+    static constexpr int A_BYTES = BM * BK * 4;
+    static constexpr int B_BYTES = BK * BN * 4;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static_assert(CONSUMERS == 256, "the register split assumes two consumer warpgroups");
+};
+
+// One producer warpgroup and two consumer warpgroups. Launched at
+// kLaunchRegs per thread, the producer warpgroup gives registers back
+// (setmaxnreg.dec to kProducerRegs) and the consumers take them
+// (setmaxnreg.inc to kConsumerRegs).
+constexpr int kProducerThreads = 128;
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 56;
+constexpr int kConsumerRegs = 224;
+static_assert(128 * kProducerRegs + 256 * kConsumerRegs <= 384 * kLaunchRegs,
+              "register split exceeds the launch allocation");
+
+__device__ __forceinline__ void producer_regs() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+}
+__device__ __forceinline__ void consumer_regs() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+}
+
+// Byte offset of A element (r, kk) inside a stage's A tile.
+__device__ __forceinline__ uint32_t a_tile_offset(int r, int kk) {
+    return static_cast<uint32_t>(r * 128 + ((((kk >> 2) ^ (r & 7)) << 4) | ((kk & 3) << 2)));
+}
+
+template <class Cfg>
+struct Accum {
+    float2 v[Cfg::TM][Cfg::TN / 2];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < Cfg::TN / 2; ++j) v[i][j] = make_float2(0.0f, 0.0f);
+    }
+    // The four outputs of row i, column group q, NaN canonicalised.
+    __device__ __forceinline__ float4 out4(int i, int q) const {
+        float4 r;
+        r.x = canonical_nan(v[i][2 * q].x);
+        r.y = canonical_nan(v[i][2 * q].y);
+        r.z = canonical_nan(v[i][2 * q + 1].x);
+        r.w = canonical_nan(v[i][2 * q + 1].y);
+        return r;
+    }
+};
+
+// All 32 k of one stage, in increasing k, for this thread's TM x TN outputs.
+template <int MODE, class Cfg>
+__device__ __forceinline__ void mma_stage(Accum<Cfg> &acc, const float *As, const float *Bs,
+                                          int arow0, int bcol0, int ty) {
+    constexpr int TM = Cfg::TM, TN = Cfg::TN, BN = Cfg::BN;
+#pragma unroll
+    for (int kc = 0; kc < Cfg::BK / 4; ++kc) {
+        float4 a[TM];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            // row arow0 + 8i has (row % 8) == ty, so its chunk kc sits at kc ^ ty
+            a[i] = *reinterpret_cast<const float4 *>(As + (arow0 + 8 * i) * 32 + ((kc ^ ty) << 2));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float4 b[TN / 4];
+#pragma unroll
+            for (int q = 0; q < TN / 4; ++q) {
+                b[q] = *reinterpret_cast<const float4 *>(Bs + (kc * 4 + kk) * BN + bcol0 + 16 * q);
+            }
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const float av = (kk == 0) ? a[i].x : (kk == 1) ? a[i].y : (kk == 2) ? a[i].z : a[i].w;
+                if constexpr (Cfg::X2) {
+                    const float2 a2 = make_float2(av, av);
+#pragma unroll
+                    for (int q = 0; q < TN / 4; ++q) {
+                        acc.v[i][2 * q] = term2<MODE>(acc.v[i][2 * q], a2, make_float2(b[q].x, b[q].y));
+                        acc.v[i][2 * q + 1] =
+                            term2<MODE>(acc.v[i][2 * q + 1], a2, make_float2(b[q].z, b[q].w));
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < TN / 4; ++q) {
+                        float2 &u = acc.v[i][2 * q];
+                        float2 &w = acc.v[i][2 * q + 1];
+                        u.x = term<MODE>(u.x, av, b[q].x);
+                        u.y = term<MODE>(u.y, av, b[q].y);
+                        w.x = term<MODE>(w.x, av, b[q].z);
+                        w.y = term<MODE>(w.y, av, b[q].w);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Output tiles in a grouped raster: kGroupM tile rows at a time, so the
+// tiles running together share A row panels and B column panels in L2.
+struct TileRaster {
+    int tiles_m, tiles_n;
+    static constexpr int kGroupM = 8;
+    __device__ __forceinline__ void at(int64_t t, int &tm, int &tn) const {
+        const int64_t per_group = static_cast<int64_t>(kGroupM) * tiles_n;
+        const int group = static_cast<int>(t / per_group);
+        const int first_m = group * kGroupM;
+        const int gsize = min(tiles_m - first_m, kGroupM);
+        const int r = static_cast<int>(t % per_group);
+        tm = first_m + r % gsize;
+        tn = r / gsize;
+    }
+};
+
+template <class Cfg>
+__device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                       ~static_cast<uintptr_t>(1023));
+}
+
+}  // namespace om

@@ -1,0 +1,187 @@
+/*
+ * om.h -- C ABI of the GB300 (sm_103a) fp32 matrix product and NCHW 2-D
+ * convolution library (libom_gpu.so).
+ *
+ * What is computed (OneModel documentation):
+ *   - "Exact mode", section "Matrix product (C = A * B, row-major, A is m x k,
+ *     B is k x n)": for every output, acc = +0; for p = 0 .. k-1 in increasing
+ *     order, acc = round(acc + round(A[i][p] * B[p][j])); a NaN result is
+ *     stored as the bits 0x7FC00000; k = 0 gives +0.
+ *   - "Matrix product and convolution kernels", section "Fast mode": the same
+ *     order (one accumulator, increasing k, from +0) with one fused
+ *     multiply-add per term.
+ *   - "Exact mode", section "Convolution (2-D, NCHW, weights [Cout, Cin/G,
+ *     KH, KW])": output (n, oc, y, x) of group g = oc / (Cout/G) sums over
+ *     c, then ky, then kx of weight[oc][c][ky][kx] * v, where
+ *     v = input[n][g*Cin/G + c][y*stride - pad + ky*dil][x*stride - pad + kx*dil]
+ *     inside the plane and +0 outside (padding taps are real products);
+ *     output size floor((size + 2*pad - dil*(K-1) - 1) / stride) + 1.
+ *   - "Exact mode", rules 1-5: binary32 round-to-nearest-even, no fused
+ *     multiply-add in exact mode, subnormals kept (no flush-to-zero), start
+ *     from +0, canonical NaN, results independent of blocking and threads.
+ *
+ * Both OM_MODE_EXACT and OM_MODE_FAST produce exactly one bit pattern per
+ * output, whatever kernel configuration, grid or stream runs the call. Fast
+ * mode also stores NaN as 0x7FC00000 (the documentation lets fast mode keep
+ * the hardware payload; this library canonicalises in both modes).
+ * OM_MODE_TF32X3 is a separate tolerance mode on the tensor cores (see
+ * om_gemm_f32); it is never bit-exact.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named A, B, C, x, w, w_packed, y are DEVICE pointers to memory
+ *     owned by the caller. The library allocates no device memory and keeps
+ *     no per-call state; it only caches device properties.
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls are asynchronous on that stream and never synchronise;
+ *     a kernel fault surfaces on the stream as CUDA reports it.
+ *   - Sizes are int64_t; every size and stride is validated on the host
+ *     before anything is launched. A call that fails validation launches
+ *     nothing and leaves every output untouched.
+ *   - Output ranges must not overlap input ranges (OM_ERR_ALIAS).
+ *   - The return value is an om_status; om_status_string() names it.
+ */
+#ifndef OM_H
+#define OM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define OM_API __attribute__((visibility("default")))
+#else
+#define OM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OM_VERSION 10000 /* 1.0.0 */
+
+typedef enum om_status {
+    OM_OK = 0,
+    OM_ERR_INVALID_ARG = 1, /* negative size, short leading dimension, stride/dil < 1, pad < 0, bad groups */
+    OM_ERR_NULL_PTR = 2,    /* NULL pointer for a non-empty operand */
+    OM_ERR_ALIAS = 3,       /* the output range overlaps an input range */
+    OM_ERR_UNSUPPORTED = 4, /* unknown mode, or a mode with no kernel for this call (reported, never approximated) */
+    OM_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+    OM_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up (see om_device_status) */
+    OM_ERR_ALIGNMENT = 7,   /* a pointer is not 4-byte aligned, or packed weights not 16-byte aligned */
+    OM_ERR_TOO_LARGE = 8    /* a size exceeds what the kernels index (see each entry point) */
+} om_status;
+
+typedef enum om_mode {
+    OM_MODE_EXACT = 0,  /* round(acc + round(a*b)), no fused multiply-add */
+    OM_MODE_FAST = 1,   /* acc = fma(a, b, acc), same order */
+    OM_MODE_TF32X3 = 2  /* tensor-core 3xTF32 split; tolerance, not bit-exact */
+} om_mode;
+
+/* Library version, OM_VERSION of the build. */
+OM_API int om_version(void);
+
+/* Static name of a status code ("OM_OK", ...); "OM_UNKNOWN" for other values. */
+OM_API const char *om_status_string(int status);
+
+/*
+ * Output size of one convolution axis:
+ *   floor((size + 2*pad - dil*(ksize-1) - 1) / stride) + 1, or 0 when the
+ * numerator is negative ("Exact mode", section "Convolution", output size).
+ * Returns -1 for invalid arguments (size < 0, ksize < 1, stride < 1, pad < 0,
+ * dil < 1) or sizes beyond 2^40.
+ */
+OM_API int64_t om_conv_out_dim(int64_t size, int64_t ksize, int64_t stride, int64_t pad, int64_t dil);
+
+/*
+ * C = A * B ("Exact mode", section "Matrix product"; "Fast mode").
+ *   A: m x k row-major, row stride lda >= k (elements).
+ *   B: k x n row-major, row stride ldb >= n.
+ *   C: m x n row-major, row stride ldc >= n. Only C[i][j] with i < m and
+ *      j < n is written; columns n .. ldc-1 are never touched.
+ *   mode: OM_MODE_EXACT, OM_MODE_FAST or OM_MODE_TF32X3.
+ * m == 0 or n == 0: OM_OK, nothing launched. k == 0: C[:m, :n] = +0.
+ * Leading dimensions are checked only where the dimension is used (lda when
+ * k > 0, ldb when k > 0, ldc always for a non-empty C).
+ * Any 4-byte alignment of A, B, C and any lda, ldb, ldc is accepted; 16-byte
+ * aligned operands with lda, ldb multiples of 4 take the TMA-fed kernel,
+ * others a kernel fed by 4-byte copies; both give identical bits.
+ * OM_MODE_TF32X3: each operand is split into a TF32 high part and a TF32
+ * low part; C accumulates hi*hi + hi*lo + lo*hi in fp32 on the tensor cores.
+ * Bound, for outputs whose exact-mode result is finite:
+ *   |C - C_exact| <= 1e-5 * sqrt(k) * sum_p |A[i][p]| * |B[p][j]|.
+ * Returns OM_ERR_UNSUPPORTED in this mode when no tensor-core kernel can run
+ * the operands' alignment.
+ */
+OM_API int om_gemm_f32(int64_t m, int64_t n, int64_t k,
+                       const float *A, int64_t lda,
+                       const float *B, int64_t ldb,
+                       float *C, int64_t ldc,
+                       int mode, void *stream);
+
+/*
+ * 2-D convolution, NCHW ("Exact mode", section "Convolution"; "Convolution
+ * (fast mode)", section "What each output is"), computed as an implicit
+ * matrix product: per image and group, A = the group's weights
+ * (Cout/G x Cin/G*KH*KW), B = the input patches gathered straight into
+ * on-chip memory with the zero border written during the gather, C = the
+ * group's output planes. Padding is never materialised.
+ *   x: [N][Cin][H][W] contiguous.
+ *   w: [Cout][Cin/G][KH][KW] contiguous.
+ *   y: [N][Cout][OutH][OutW] contiguous, OutH/OutW from om_conv_out_dim.
+ *   Symmetric padding pad, one stride and one dilation for both axes.
+ *   G >= 1 must divide Cin and Cout (depthwise, G == Cin, included).
+ *   mode: OM_MODE_EXACT or OM_MODE_FAST (OM_MODE_TF32X3 -> OM_ERR_UNSUPPORTED).
+ * An empty output (N, Cout, OutH or OutW zero) returns OM_OK with nothing
+ * launched. Cin == 0 (an empty sum) writes +0 everywhere. No bias is added.
+ * Element counts of x, w and y must each stay below 2^62; a per-image plane
+ * block (Cin*H*W or Cout*OutH*OutW) and K = Cin/G*KH*KW must stay below
+ * 2^31 (OM_ERR_TOO_LARGE otherwise).
+ */
+OM_API int om_conv2d_f32(int64_t N, int64_t Cin, int64_t H, int64_t W,
+                         int64_t Cout, int64_t G, int64_t KH, int64_t KW,
+                         int64_t stride, int64_t pad, int64_t dil,
+                         const float *x, const float *w, float *y,
+                         int mode, void *stream);
+
+/*
+ * Re-lays out convolution weights once for om_conv2d_f32_packed
+ * ("Convolution (fast mode)", section "Layout of the work": weights packed
+ * once, when the model is loaded).
+ * Layout written: for each group g, a (Cout/G) x Kp row-major block with
+ * Kp = K rounded up to a multiple of 4 (K = Cin/G*KH*KW), columns K..Kp-1
+ * set to +0; groups follow one another. Every row then starts on a 16-byte
+ * boundary, which lets the convolution fetch weights with TMA.
+ * Two-call convention: with w_packed == NULL, only *packed_bytes is set
+ * (the size the caller must allocate) and nothing is launched. Otherwise
+ * *packed_bytes (if packed_bytes != NULL) is set again, and the packing
+ * kernel is launched on stream. w_packed must be 16-byte aligned.
+ */
+OM_API int om_pack_conv_weights(int64_t Cout, int64_t Cin, int64_t G, int64_t KH, int64_t KW,
+                                const float *w, float *w_packed, size_t *packed_bytes,
+                                void *stream);
+
+/*
+ * om_conv2d_f32 with weights already packed by om_pack_conv_weights (same
+ * Cout, Cin, G, KH, KW). The result is bit-identical to om_conv2d_f32 on the
+ * unpacked weights. w_packed must be 16-byte aligned (OM_ERR_ALIGNMENT).
+ */
+OM_API int om_conv2d_f32_packed(int64_t N, int64_t Cin, int64_t H, int64_t W,
+                                int64_t Cout, int64_t G, int64_t KH, int64_t KW,
+                                int64_t stride, int64_t pad, int64_t dil,
+                                const float *x, const float *w_packed, float *y,
+                                int mode, void *stream);
+
+/*
+ * Synchronises stream, then reads and clears the library's device status
+ * words for the current device. Every device-side wait in the library's
+ * kernels (mbarrier waits of the TMA and tensor-core pipelines) is bounded;
+ * a wait that runs out records OM_ERR_TIMEOUT there and the kernel returns
+ * early instead of hanging. Returns OM_OK, OM_ERR_TIMEOUT, or OM_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+OM_API int om_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OM_H */

@@ -1,0 +1,129 @@
+"""GPU parity of om_conv2d_f32 / om_conv2d_f32_packed against the oracle, bit for bit."""
+import numpy as np
+import pytest
+
+import implicit_gemm_convolution_gb300 as om
+import oracle
+from implicit_gemm_convolution_gb300 import synth
+from tests.gpu_util import (assert_bits_equal, forced_config, guarded_output, guards_intact, sha,
+                            to_dev)
+
+pytestmark = pytest.mark.gpu
+
+MODES = [(oracle.EXACT, "exact"), (oracle.FAST, "fast")]
+CFGS = [0, None]  # direct kernel, default dispatch
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    om.build()
+    om.lib()
+    oracle.build()
+
+
+def run_conv(c: synth.ConvCase, name, cfg=None, packed=False):
+    import torch
+    x, w = to_dev(c.x), to_dev(c.w)
+    OH = oracle.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.pad, c.dil)
+    OW = oracle.conv_out_dim(c.W, c.KW, c.stride, c.pad, c.pad, c.dil)
+    init = np.zeros((c.N, c.Cout, OH, OW), np.float32)
+    init.view(np.uint32)[:] = 0x7FBADBAD
+    buf, y = guarded_output(init)
+    with forced_config("OM_FORCE_CONV_CFG", cfg):
+        if packed:
+            wp = om.pack_conv_weights(w, c.G)
+            st = om.lib().om_conv2d_f32_packed(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW,
+                                               c.stride, c.pad, c.dil, x.data_ptr(), wp.data_ptr(),
+                                               y.data_ptr(), om.MODES[name], None)
+        else:
+            st = om.lib().om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride,
+                                        c.pad, c.dil, x.data_ptr(), w.data_ptr(), y.data_ptr(),
+                                        om.MODES[name], None)
+    assert st == 0, om.STATUS_NAMES.get(st, st)
+    torch.cuda.synchronize()
+    assert om.device_status() == 0
+    assert guards_intact(buf), "write outside y"
+    return y.cpu().numpy().reshape(init.shape)
+
+
+def want_conv(c, mode, images=None):
+    x = c.x if images is None else c.x[images[0]:images[1]]
+    return oracle.conv2d(x, c.w, c.stride, c.pad, c.dil, c.G, mode, oracle.default_threads())
+
+
+SMALL = [
+    # N, Cin, H, W, Cout, G, KH, KW, s, p, d
+    (2, 3, 7, 6, 4, 1, 3, 3, 1, 1, 1),
+    (1, 4, 9, 9, 6, 2, 3, 2, 2, 1, 2),
+    (2, 8, 5, 5, 8, 8, 3, 3, 1, 2, 1),
+    (1, 6, 11, 4, 3, 3, 1, 1, 1, 0, 1),
+    (3, 2, 4, 9, 5, 1, 2, 3, 3, 0, 1),
+    (2, 16, 12, 12, 64, 1, 3, 3, 1, 1, 1),
+    (3, 32, 10, 10, 96, 2, 1, 1, 1, 0, 1),
+    (2, 40, 13, 11, 70, 1, 3, 3, 2, 1, 1),
+    (1, 3, 30, 30, 16, 1, 7, 7, 2, 3, 1),
+    (4, 64, 7, 7, 128, 1, 3, 3, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL)
+@pytest.mark.parametrize("cfg", CFGS)
+@pytest.mark.parametrize("mode,name", MODES)
+def test_small_convs(shape, mode, name, cfg):
+    c = synth.make_conv("t", *shape, seed=sum(shape), dist_x=("uniform", -1, 1),
+                        dist_w=("normal", 0, 0.5))
+    assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"{shape} {name} cfg={cfg}")
+
+
+@pytest.mark.parametrize("shape", SMALL[:6])
+@pytest.mark.parametrize("mode,name", MODES)
+def test_packed_equals_unpacked(shape, mode, name):
+    c = synth.make_conv("t", *shape, seed=3 + sum(shape))
+    a = run_conv(c, name, None, packed=False)
+    b = run_conv(c, name, None, packed=True)
+    assert sha(a) == sha(b)
+    assert_bits_equal(a, want_conv(c, mode))
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_padding_taps_with_nonfinite_weights(mode, name):
+    c = synth.make_conv("t", 2, 4, 6, 6, 4, 1, 3, 3, 1, 1, 1, seed=8)
+    c.w[1, 2, 0, 0] = np.inf
+    c.w[3, 0, 2, 2] = np.nan
+    for cfg in CFGS:
+        assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"nonfinite cfg={cfg}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_grouped_strided_dilated_workload(mode, name):
+    c = synth.workload_conv_grouped()
+    for cfg in CFGS:
+        assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"grouped cfg={cfg}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_conv3x3_workload_sampled_images(mode, name):
+    c = synth.workload_conv3x3()
+    got = run_conv(c, name)
+    for n0 in (0, 31):
+        assert_bits_equal(got[n0:n0 + 1], want_conv(c, mode, (n0, n0 + 1)), f"conv3x3 image {n0}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_conv1x1_workload_sampled_images(mode, name):
+    c = synth.workload_conv1x1()
+    got = run_conv(c, name)
+    for n0 in (0, 17):
+        assert_bits_equal(got[n0:n0 + 1], want_conv(c, mode, (n0, n0 + 1)), f"conv1x1 image {n0}")
+
+
+def test_empty_input_channels_give_plus_zero():
+    import torch
+    x = torch.zeros((2, 0, 5, 5), device="cuda")
+    w = torch.zeros((3, 0, 3, 3), device="cuda")
+    y = torch.full((2, 3, 5, 5), 7.0, device="cuda")
+    st = om.lib().om_conv2d_f32(2, 0, 5, 5, 3, 1, 3, 3, 1, 1, 1, x.data_ptr(), w.data_ptr(),
+                                y.data_ptr(), 0, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert (y.cpu().numpy().view(np.uint32) == 0).all()
