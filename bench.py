@@ -46,23 +46,43 @@ def fp32_peak_tflops(sms: int, exact: bool) -> float:
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+    """nvidia-smi clock/throttle samples, each stamped with the host time it
+    arrived; summary() keeps the samples taken inside a given time window."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.out = ""
+        self.samples = []  # (host time, sm MHz, max MHz, set of active reasons)
+        self.reader = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            active = {n for n, v in zip(self.REASONS, parts[5:9]) if v.lower() == "active"}
+            self.samples.append((time.time(), sm, mx, active))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 5.0:
+                time.sleep(0.05)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -71,30 +91,27 @@ class ClockSampler:
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+            if self.reader is not None:
+                self.reader.join(timeout=5)
 
-    def summary(self) -> dict:
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1 + 0.15]
+        basis = "inside the timed region"
+        if not inside:
+            after = [s for s in self.samples if s[0] >= t0]
+            inside = after[:1]
+            basis = "first sample after the timed region began (region shorter than the sampling period)"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for s in inside:
+            reasons |= s[3]
+        return {"sm_mhz": float(np.median([s[1] for s in inside])),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "basis": basis}
 
 
 # ----------------------------------------------------------------- workloads
@@ -191,20 +208,25 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clocks:
-        t_wall0 = time.perf_counter()
-        kernel_ms = []
-        for _ in range(args.steps):
-            flush()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            step_exact()
-            e1.record(stream)
-            e1.synchronize()
-            kernel_ms.append(e0.elapsed_time(e1))
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+    clocks = ClockSampler(local_rank)
+    clocks.__enter__()
+    region0 = time.time()
+    t_wall0 = time.perf_counter()
+    kernel_ms = []
+    for _ in range(args.steps):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step_exact()
+        e1.record(stream)
+        e1.synchronize()
+        kernel_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    region1 = time.time()
+    clock_summary = clocks.summary(region0, region1)
+    clocks.__exit__(None, None, None)
     ms_local = float(np.mean(kernel_ms))
     ms = ms_local
     if dist is not None:
@@ -316,7 +338,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clock_summary,
         "wall_s_timed_region": round(t_wall, 3),
         "modes": extras,
     }
@@ -383,7 +405,7 @@ def run_reference(args, rank: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--extra-steps", type=int, default=5)

@@ -3,7 +3,8 @@
 Each translation unit under csrc/ compiles to an object in parallel, then
 nvcc links the shared library into ``_lib/``. Flags: one -gencode for
 sm_103a, -lineinfo, -O3, -fmad=false (no contraction of a*b+c anywhere; the
-kernels also use explicitly rounded intrinsics), and no -ftz / fast-math, so
+kernels also use explicitly rounded intrinsics; the same switch is passed to
+ptxas), and no -ftz / fast-math, so
 subnormals are computed and every operation rounds to nearest even.
 """
 from __future__ import annotations
@@ -23,7 +24,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libom_gpu.so")
 
 SOURCES = ["om_api.cu", "simple_kernels.cu", "sgemm_tiled.cu", "conv_implicit.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-fmad=false",
+NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-fmad=false", "-Xptxas", "--fmad=false",
                      "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                      f"-I{INCLUDE}", "-Xptxas", "-v"]
 

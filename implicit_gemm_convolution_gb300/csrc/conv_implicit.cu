@@ -1,14 +1,343 @@
-// conv_implicit.cu -- implicit-GEMM convolution (every call currently falls
-// back to the direct kernel).
-#include "om_device.cuh"
+// conv_implicit.cu -- NCHW 2-D convolution as an implicit matrix product on
+// the CUDA cores of sm_103a, bit-exact in both modes.
+//
+// What each output is ("Exact mode" page, section "Convolution"; "Convolution
+// (fast mode)" page, section "What each output is"): output (n, oc, oy, ox)
+// of group g sums, for taps p = (c*KH + ky)*KW + kx in increasing order, the
+// term w[oc][c][ky][kx] * v with
+//   v = x[n][g*Cin/G + c][oy*s - pad + ky*d][ox*s - pad + kx*d]
+// inside the plane and +0 outside; padding taps are real products, so an
+// infinite or NaN weight meeting padding gives NaN. NaN is stored as
+// 0x7FC00000.
+//
+// The product per group g ("Convolution (fast mode)", section "Layout of the
+// work"): A = the group's weights, Cout/G rows by K = Cin/G*KH*KW taps; B = the
+// patches, K rows by N*OutH*OutW columns (all images of the call side by side:
+// every output is independent, so merging images changes no bit); C = the
+// group's output planes. B is never built: the producer warpgroup gathers each
+// 32-tap x BN-column strip straight from the input planes into shared memory
+// with 4-byte cp.async, writing +0 (src-size 0) for taps outside the plane --
+// the zero border is written during the gather, never materialised. Weight
+// tiles come by TMA when the weight rows are 16-byte aligned (always for the
+// packed layout), else by 4-byte cp.async. The consumer warpgroups run the
+// same register-tile loop as the matrix product (simt_tile.cuh), so every
+// output accumulates its taps in order from +0 in one thread's registers.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "om_internal.h"
+#include "simt_tile.cuh"
 
 namespace om {
 
 __device__ unsigned g_status_conv;
 
-cudaError_t launch_conv_implicit(const ConvProblem &, int, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+// Geometry the kernel reads (all per-image quantities fit in 32 bits; the
+// host validated Cin*H*W, Cout*OH*OW and K below 2^31).
+struct ConvGeom {
+    const float *x;
+    const float *w;
+    float *y;
+    int64_t ncols;  // N * OH * OW
+    int H, W, HW, OH, OW, P;  // P = OH*OW
+    int Cin, Cout, cin_g, M;  // M = Cout/G
+    int KH, KW, sH, sW, pT, pL, dH, dW;
+    int K, w_ld;
+    int tiles_m, tiles_n, G;
+};
+
+__device__ __forceinline__ void conv_record_timeout(int *abort_flag) {
+    atomicOr(&g_status_conv, kDevErrTimeout);
+    *reinterpret_cast<volatile int *>(abort_flag) = 1;
+}
+
+// Tile t -> (m tile, column tile, group); the m tiles of one column strip are
+// adjacent so they run together and share the gathered input through L2.
+__device__ __forceinline__ void conv_tile(const ConvGeom &g, int64_t t, int &tm, int64_t &tn,
+                                          int &grp) {
+    tm = static_cast<int>(t % g.tiles_m);
+    const int64_t r = t / g.tiles_m;
+    tn = r % g.tiles_n;
+    grp = static_cast<int>(r / g.tiles_n);
+}
+
+template <class Cfg, bool A_TMA>
+__device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMap *mapW,
+                                             uint8_t *smem, uint64_t *full, uint64_t *empty,
+                                             int *abort_flag, int64_t total, int nk, int pt) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
+    constexpr int CPT = BN / kProducerThreads;  // gathered columns per producer thread
+    static_assert(BN % kProducerThreads == 0, "columns split evenly over the producer");
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+        int tm, grp;
+        int64_t tn;
+        conv_tile(g, t, tm, tn, grp);
+        // Per gathered column: the group's first input plane of its image and
+        // the input coordinates of tap (0, 0).
+        const float *base[CPT];
+        int iy0[CPT], ix0[CPT];
+        bool cvalid[CPT];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int64_t col = tn * BN + pt + kProducerThreads * j;
+            cvalid[j] = col < g.ncols;
+            const int64_t img = cvalid[j] ? col / g.P : 0;
+            const int pix = cvalid[j] ? static_cast<int>(col - img * g.P) : 0;
+            const int oy = pix / g.OW, ox = pix - (pix / g.OW) * g.OW;
+            base[j] = g.x + (img * g.Cin + static_cast<int64_t>(grp) * g.cin_g) * g.HW;
+            iy0[j] = oy * g.sH - g.pT;
+            ix0[j] = ox * g.sW - g.pL;
+        }
+        const int row0 = grp * g.M + tm * BM;  // first weight row of the tile
+        // tap state of the first tap of the stage: p = (c*KH + ky)*KW + kx
+        int c = 0, ky = 0, kx = 0;
+        for (int kt = 0; kt < nk; ++kt) {
+            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                conv_record_timeout(abort_flag);
+                cp_async_wait_all();
+                if (A_TMA && pt == 0) {
+                    // let the weight tiles already requested land first
+                    for (int s2 = 0; s2 < Cfg::STAGES; ++s2) {
+                        if (issued > s2) {
+                            const int64_t last = s2 + ((issued - 1 - s2) / Cfg::STAGES) * Cfg::STAGES;
+                            (void)mbar_wait(&full[s2], static_cast<uint32_t>((last / Cfg::STAGES) & 1));
+                        }
+                    }
+                }
+                return;
+            }
+            ++issued;
+            uint8_t *sa = smem + stage * Cfg::STAGE_BYTES;
+            const uint32_t sa32 = smem_u32(sa);
+            const uint32_t sb32 = sa32 + Cfg::A_BYTES;
+            if constexpr (A_TMA) {
+                if (pt == 0) {
+                    mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES);
+                    tma_load_2d(sa, mapW, &full[stage], kt * BK, row0);
+                }
+            } else {
+                // rows of this group only; +0 past the group's rows and past K
+                const int kk = pt % 32;
+                const int p = kt * BK + kk;
+                for (int r = pt / 32; r < BM; r += 4) {
+                    const int mrow = tm * BM + r;
+                    const bool ok = (mrow < g.M) && (p < g.K);
+                    const float *src = ok ? g.w + static_cast<int64_t>(row0 + r) * g.w_ld + p : g.w;
+                    cp_async_4(sa32 + a_tile_offset(r, kk), src, ok ? 4u : 0u);
+                }
+            }
+            // Gather the 32 taps of this stage for the thread's columns.
+#pragma unroll 4
+            for (int kk = 0; kk < BK; ++kk) {
+                const int p = kt * BK + kk;
+                const bool tap_ok = p < g.K;
+                const int dy = ky * g.dH, dx = kx * g.dW;
+                const int plane = tap_ok ? c * g.HW : 0;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    const int iy = iy0[j] + dy, ix = ix0[j] + dx;
+                    const bool ok = tap_ok && cvalid[j] && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
+                                    static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
+                    const float *src = ok ? base[j] + (plane + iy * g.W + ix) : g.x;
+                    cp_async_4(sb32 + (kk * BN + pt + kProducerThreads * j) * 4, src, ok ? 4u : 0u);
+                }
+                if (++kx == g.KW) {
+                    kx = 0;
+                    if (++ky == g.KH) {
+                        ky = 0;
+                        ++c;
+                    }
+                }
+            }
+            cp_async_arrive_noinc(&full[stage]);
+            if (++stage == Cfg::STAGES) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+    }
+    cp_async_wait_all();
+}
+
+template <int MODE, class Cfg, bool A_TMA>
+__global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
+    conv_implicit_kernel(const __grid_constant__ CUtensorMap mapW, ConvGeom g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = aligned_smem<Cfg>(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+    uint64_t *empty = full + Cfg::STAGES;
+    int *abort_flag = reinterpret_cast<int *>(empty + Cfg::STAGES);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            // every producer thread arrives after its copies land; with TMA
+            // weights, producer thread 0 also arrives with the byte count
+            mbar_init(&full[s], kProducerThreads + (A_TMA ? 1 : 0));
+            mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+
+    const int64_t total = static_cast<int64_t>(g.tiles_m) * g.tiles_n * g.G;
+    const int nk = (g.K + Cfg::BK - 1) / Cfg::BK;
+
+    if (warp >= Cfg::CONSUMER_WARPS) {
+        producer_regs();
+        if constexpr (A_TMA) {
+            if (threadIdx.x == Cfg::CONSUMERS) prefetch_tensormap(&mapW);
+        }
+        conv_produce<Cfg, A_TMA>(g, &mapW, smem, full, empty, abort_flag, total, nk,
+                                 threadIdx.x - Cfg::CONSUMERS);
+        return;
+    }
+
+    consumer_regs();
+    const int ty = lane / 4, tx = lane % 4;
+    const int arow0 = (warp / Cfg::WARPS_N) * Cfg::WM + ty;
+    const int bcol0 = (warp % Cfg::WARPS_N) * Cfg::WN + tx * 4;
+    const bool vec_ok = (g.P % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.y) & 15) == 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+        int tm, grp;
+        int64_t tn;
+        conv_tile(g, t, tm, tn, grp);
+        Accum<Cfg> acc;
+        acc.zero();
+        for (int kt = 0; kt < nk; ++kt) {
+            if (!mbar_wait(&full[stage], phase)) {
+                conv_record_timeout(abort_flag);
+                return;
+            }
+            const float *As = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE_BYTES);
+            const float *Bs = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE_BYTES + Cfg::A_BYTES);
+            mma_stage<MODE, Cfg>(acc, As, Bs, arow0, bcol0, ty);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == Cfg::STAGES) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        // Epilogue: row i of the tile is output channel grp*M + tm*BM + i,
+        // column j is (image, pixel) = divmod(j, OH*OW).
+#pragma unroll
+        for (int q = 0; q < Cfg::TN / 4; ++q) {
+            const int64_t col = tn * Cfg::BN + bcol0 + 16 * q;
+            if (col >= g.ncols) continue;
+            const int64_t img = col / g.P;
+            const int pix = static_cast<int>(col - img * g.P);
+            const bool vec = vec_ok && (col + 3 < g.ncols);
+#pragma unroll
+            for (int i = 0; i < Cfg::TM; ++i) {
+                const int mrow = tm * Cfg::BM + arow0 + 8 * i;
+                if (mrow >= g.M) continue;
+                const int oc = grp * g.M + mrow;
+                const float4 v = acc.out4(i, q);
+                float *dst = g.y + (img * g.Cout + oc) * static_cast<int64_t>(g.P) + pix;
+                if (vec) {
+                    *reinterpret_cast<float4 *>(dst) = v;
+                } else {
+                    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int64_t cu = col + u;
+                        if (cu >= g.ncols) break;
+                        const int64_t iu = cu / g.P;
+                        const int64_t pu = cu - iu * g.P;
+                        g.y[(iu * g.Cout + oc) * static_cast<int64_t>(g.P) + pu] = e[u];
+                    }
+                }
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 conv_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        }
+    }
+    return fn;
+}
+
+// Weight matrix Cout x K (row stride w_ld), box 32 taps x BM rows, 128B
+// swizzle; taps >= K and rows >= Cout read as +0.
+static bool make_weight_map(CUtensorMap *map, const ConvProblem &p, int box_rows) {
+    auto fn = conv_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.Cout)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.w_ld) * 4};
+    cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(p.w), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+using ConvCfg64x256 = TileCfg<64, 256, 8, 8, 1, 8, 4, true>;
+
+template <int MODE, class Cfg>
+static cudaError_t launch_conv_cfg(const ConvProblem &p, cudaStream_t s) {
+    ConvGeom g;
+    g.x = p.x; g.w = p.w; g.y = p.y;
+    g.ncols = p.N * p.OH * p.OW;
+    g.H = static_cast<int>(p.H); g.W = static_cast<int>(p.W); g.HW = static_cast<int>(p.H * p.W);
+    g.OH = static_cast<int>(p.OH); g.OW = static_cast<int>(p.OW); g.P = static_cast<int>(p.OH * p.OW);
+    g.Cin = static_cast<int>(p.Cin); g.Cout = static_cast<int>(p.Cout);
+    g.cin_g = static_cast<int>(p.Cin / p.G); g.M = static_cast<int>(p.Cout / p.G);
+    g.KH = static_cast<int>(p.KH); g.KW = static_cast<int>(p.KW);
+    g.sH = static_cast<int>(p.sH); g.sW = static_cast<int>(p.sW);
+    g.pT = static_cast<int>(p.pT); g.pL = static_cast<int>(p.pL);
+    g.dH = static_cast<int>(p.dH); g.dW = static_cast<int>(p.dW);
+    g.K = static_cast<int>(p.K); g.w_ld = static_cast<int>(p.w_ld);
+    g.G = static_cast<int>(p.G);
+    const int64_t tiles_m = (g.M + Cfg::BM - 1) / Cfg::BM;
+    const int64_t tiles_n = (g.ncols + Cfg::BN - 1) / Cfg::BN;
+    if (tiles_n > 0x7FFFFFFF || p.w_ld > 0x7FFFFFFF) return cudaErrorNotSupported;
+    g.tiles_m = static_cast<int>(tiles_m);
+    g.tiles_n = static_cast<int>(tiles_n);
+    const int64_t total = tiles_m * tiles_n * p.G;
+    const int64_t grid = total < num_sms() ? total : num_sms();
+
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    const bool a_tma = ((reinterpret_cast<uintptr_t>(p.w) & 15) == 0) && (p.w_ld % 4 == 0) &&
+                       make_weight_map(&map, p, Cfg::BM);
+    cudaError_t e;
+    if (a_tma) {
+        auto kernel = conv_implicit_kernel<MODE, Cfg, true>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        kernel<<<static_cast<unsigned>(grid), Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s>>>(map, g);
+    } else {
+        auto kernel = conv_implicit_kernel<MODE, Cfg, false>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        kernel<<<static_cast<unsigned>(grid), Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s>>>(map, g);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, cudaStream_t s) {
+    if (cfg != kConvAuto && cfg != kConvImplicit) return cudaErrorNotSupported;
+    if (p.K == 0) return cudaErrorNotSupported;
+    return mode == kFast ? launch_conv_cfg<kFast, ConvCfg64x256>(p, s)
+                         : launch_conv_cfg<kExact, ConvCfg64x256>(p, s);
 }
 
 cudaError_t read_clear_status_conv(unsigned *out, cudaStream_t s) {

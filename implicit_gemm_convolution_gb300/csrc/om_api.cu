@@ -92,6 +92,10 @@ int validate_conv(const ConvArgs &a, const float *x, const float *w, bool packed
     if (a.H > lim31 || a.W > lim31 || a.KH > 65535 || a.KW > 65535 || a.stride > 65535 ||
         a.dil > 65535 || a.pad > 65535)
         return OM_ERR_TOO_LARGE;
+    // input coordinates oy*s - pad + ky*d stay inside 32-bit integers
+    if (a.H + 2 * a.pad >= lim31 || a.W + 2 * a.pad >= lim31 ||
+        (a.KH - 1) * a.dil >= lim31 - a.H || (a.KW - 1) * a.dil >= lim31 - a.W)
+        return OM_ERR_TOO_LARGE;
     const int64_t OH = out_dim(a.H, a.KH, a.stride, a.pad, a.dil);
     const int64_t OW = out_dim(a.W, a.KW, a.stride, a.pad, a.dil);
     const int64_t cin_g = a.Cin / a.G;

@@ -39,14 +39,56 @@ __device__ __forceinline__ float term(float acc, float a, float b) {
     }
 }
 
-// Two independent outputs at once (paired-lane fp32 instructions of sm_100+).
-// Each lane is rounded on its own exactly like the scalar form above.
+// Paired-lane fp32 instructions of sm_100+ (inline PTX, explicit .rn).
+// Fast mode uses the paired fused multiply-add: one rounding per lane.
+// Exact mode must keep the multiply and the add as two roundings. The
+// assembler was measured to contract a paired multiply followed by a paired
+// add into the paired fused multiply-add even when both carry .rn and even
+// with --fmad=false, so exact mode pairs only the add: two scalar
+// mul.rn.f32 (never contracted) feed one add.rn.f32x2. That form was checked
+// bit for bit against the all-scalar form on the device and costs three
+// issue slots per two terms instead of four.
+__device__ __forceinline__ float mul_rn_scalar(float a, float b) {
+    float r;
+    asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+    unsigned long long r;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%1, %2};\n\t"
+        "mov.b64 rb, {%3, %4};\n\t"
+        "add.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(r)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+    unsigned long long r;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%1, %2};\n\t"
+        "mov.b64 rb, {%3, %4};\n\t"
+        "mov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+        : "=l"(r)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+
+// Two independent outputs: acc.x gets a.x*b.x, acc.y gets a.y*b.y, each lane
+// rounded exactly like term<MODE>.
 template <int MODE>
 __device__ __forceinline__ float2 term2(float2 acc, float2 a, float2 b) {
     if constexpr (MODE == kFast) {
-        return __ffma2_rn(a, b, acc);
+        return fma2_rn(a, b, acc);
     } else {
-        return __fadd2_rn(acc, __fmul2_rn(a, b));
+        return add2_rn(acc, make_float2(mul_rn_scalar(a.x, b.x), mul_rn_scalar(a.y, b.y)));
     }
 }
 
