@@ -402,6 +402,51 @@ def run_reference(args, rank: int):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_profile(args):
+    """Only the named workload's kernel launches (warm-up, then --steps), for
+    ncu captures: no L2 flush kernels, no extra workloads, no host baseline."""
+    import torch
+    import implicit_gemm_convolution_gb300 as om
+    from implicit_gemm_convolution_gb300 import synth
+    om.build()
+    L = om.lib()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    name, mode = args.profile.split(":")[:2]
+    gemms = {"gemm_4096^3": synth.workload_gemm_4096,
+             "gemm_prefill": lambda: synth.workload_gemm_prefill(False),
+             "gemm_prefill_ragged": lambda: synth.workload_gemm_prefill(True)}
+    convs = {"conv3x3": synth.workload_conv3x3, "conv1x1": synth.workload_conv1x1,
+             "conv_grouped": synth.workload_conv_grouped}
+    if name in gemms:
+        case = gemms[name]()
+        A = torch.from_numpy(case.A).to(dev)
+        B = torch.from_numpy(case.B).to(dev)
+        C = torch.from_numpy(case.C_init).to(dev)
+
+        def f():
+            st = om.gemm_raw(case.m, case.n, case.k, A.data_ptr(), case.lda, B.data_ptr(),
+                             case.ldb, C.data_ptr(), case.ldc, mode, stream)
+            assert st == 0, st
+    else:
+        c = convs[name]()
+        x = torch.from_numpy(c.x).to(dev)
+        w = torch.from_numpy(c.w).to(dev)
+        OH = om.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.dil)
+        OW = om.conv_out_dim(c.W, c.KW, c.stride, c.pad, c.dil)
+        y = torch.empty((c.N, c.Cout, OH, OW), dtype=torch.float32, device=dev)
+
+        def f():
+            st = L.om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad,
+                                 c.dil, x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[mode],
+                                 stream.cuda_stream)
+            assert st == 0, st
+    for _ in range(args.warmup + args.steps):
+        f()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,7 +456,13 @@ def main():
     ap.add_argument("--extra-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    help="workload:mode (gemm_4096^3, gemm_prefill, gemm_prefill_ragged, conv3x3,"
+                         " conv1x1, conv_grouped) -- launch only that kernel, for ncu")
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -33,6 +33,9 @@ namespace om {
 
 __device__ unsigned g_status_conv;
 
+// Registers of a producer thread (the gather keeps per-column state).
+constexpr int CONV_PRODUCER_REGS = 72;
+
 // Geometry the kernel reads (all per-image quantities fit in 32 bits; the
 // host validated Cin*H*W, Cout*OH*OW and K below 2^31).
 struct ConvGeom {
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     const int nk = (g.K + Cfg::BK - 1) / Cfg::BK;
 
     if (warp >= Cfg::CONSUMER_WARPS) {
-        producer_regs();
+        RegSplit<CONV_PRODUCER_REGS>::producer();
         if constexpr (A_TMA) {
             if (threadIdx.x == Cfg::CONSUMERS) prefetch_tensormap(&mapW);
         }
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
         return;
     }
 
-    consumer_regs();
+    RegSplit<CONV_PRODUCER_REGS>::consumer();
     const int ty = lane / 4, tx = lane % 4;
     const int arow0 = (warp / Cfg::WARPS_N) * Cfg::WM + ty;
     const int bcol0 = (warp % Cfg::WARPS_N) * Cfg::WN + tx * 4;

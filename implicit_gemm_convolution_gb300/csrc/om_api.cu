@@ -133,6 +133,19 @@ int validate_conv(const ConvArgs &a, const float *x, const float *w, bool packed
     return OM_OK;
 }
 
+// Output tiles are handed to a persistent grid of one CTA per SM, so a
+// launch costs whole rounds of tiles. Pick the tile shape with the smaller
+// number of rounds times tile size (ties go to the larger tile, which reuses
+// each operand load over more outputs).
+int pick_gemm_cfg(const GemmProblem &p) {
+    const int64_t sms = om::num_sms();
+    const int64_t tm = (p.m + 127) / 128;
+    const int64_t t256 = tm * ((p.n + 255) / 256), t128 = tm * ((p.n + 127) / 128);
+    const int64_t c256 = (t256 + sms - 1) / sms * 2;  // in units of a 128 x 128 tile
+    const int64_t c128 = (t128 + sms - 1) / sms;
+    return c128 < c256 ? om::kCfgTma128x128 : om::kCfgTma128x256;
+}
+
 int run_conv(const ConvProblem &p, int mode, cudaStream_t s) {
     int cfg = forced("OM_FORCE_CONV_CFG");
     if (cfg == om::kConvNaive || p.K == 0) return from_cuda(om::launch_conv_naive(p, mode, s));
@@ -195,7 +208,7 @@ int om_gemm_f32(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, co
     if (cfg > 0) {
         e = om::launch_gemm_tiled(p, mode, cfg, s);
     } else {
-        e = om::launch_gemm_tiled(p, mode, om::kCfgTma128x256, s);
+        e = om::launch_gemm_tiled(p, mode, pick_gemm_cfg(p), s);
         if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, mode, om::kCfgAsync128x128, s);
     }
     if (e == cudaErrorNotSupported) e = om::launch_gemm_naive(p, mode, s);

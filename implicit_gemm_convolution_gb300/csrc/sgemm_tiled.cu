@@ -47,12 +47,12 @@ __device__ __forceinline__ void record_timeout(int *abort_flag) {
 template <class Cfg>
 __device__ __forceinline__ void produce_tma(const CUtensorMap *mapA, const CUtensorMap *mapB,
                                             uint8_t *smem, uint64_t *full, uint64_t *empty,
-                                            int *abort_flag, const TileRaster &rs, int64_t total,
+                                            int *abort_flag, const TileRaster &rs, int total,
                                             int nk) {
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
         int tm, tn;
         rs.at(t, tm, tn);
         for (int kt = 0; kt < nk; ++kt) {
@@ -87,14 +87,14 @@ __device__ __forceinline__ void produce_tma(const CUtensorMap *mapA, const CUten
 template <class Cfg>
 __device__ __forceinline__ void produce_async(const GemmProblem &p, uint8_t *smem,
                                               uint64_t *full, uint64_t *empty, int *abort_flag,
-                                              const TileRaster &rs, int64_t total, int nk,
+                                              const TileRaster &rs, int total, int nk,
                                               int pt) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
     int stage = 0;
     uint32_t phase = 0;
     const int kk_a = pt % 32;
     const int r_a0 = pt / 32;  // 0..3
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
         int tm, tn;
         rs.at(t, tm, tn);
         const int64_t m0 = static_cast<int64_t>(tm) * BM, n0 = static_cast<int64_t>(tn) * BN;
@@ -159,11 +159,11 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     }
     __syncthreads();
 
-    const int64_t total = static_cast<int64_t>(rs.tiles_m) * rs.tiles_n;
+    const int total = rs.tiles_m * rs.tiles_n;
     const int nk = static_cast<int>((p.k + Cfg::BK - 1) / Cfg::BK);
 
     if (warp >= Cfg::CONSUMER_WARPS) {
-        producer_regs();
+        RegSplit<(PROD == kProdTma ? 24 : 56)>::producer();
         if constexpr (PROD == kProdTma) {
             if (warp == Cfg::CONSUMER_WARPS && lane == 0) {
                 prefetch_tensormap(&mapA);
@@ -178,13 +178,13 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     }
 
     // Consumer warps.
-    consumer_regs();
+    RegSplit<(PROD == kProdTma ? 24 : 56)>::consumer();
     const int ty = lane / 4, tx = lane % 4;
     const int arow0 = (warp / Cfg::WARPS_N) * Cfg::WM + ty;
     const int bcol0 = (warp % Cfg::WARPS_N) * Cfg::WN + tx * 4;
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
         int tm, tn;
         rs.at(t, tm, tn);
         Accum<Cfg> acc;
@@ -283,7 +283,7 @@ static cudaError_t launch_cfg(const GemmProblem &p, cudaStream_t s) {
         if (!make_map_2d(&mapB, p.B, p.k, p.n, p.ldb, Cfg::BN, Cfg::BK, false)) return cudaErrorNotSupported;
     }
     const int64_t tm = (p.m + Cfg::BM - 1) / Cfg::BM, tn = (p.n + Cfg::BN - 1) / Cfg::BN;
-    if (tm > 0x7FFFFFFF || tn > 0x7FFFFFFF || p.k > 0x7FFFFFFF) return cudaErrorNotSupported;
+    if (tm * tn > 0x7FFFFFFF || p.k > 0x7FFFFFFF) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;

@@ -42,21 +42,27 @@ struct TileCfg {
 
 // One producer warpgroup and two consumer warpgroups. Launched at
 // kLaunchRegs per thread, the producer warpgroup gives registers back
-// (setmaxnreg.dec to kProducerRegs) and the consumers take them
-// (setmaxnreg.inc to kConsumerRegs).
+// (setmaxnreg.dec) and the consumers take them (setmaxnreg.inc): a TMA
+// producer needs almost none, a gathering producer keeps per-column state.
 constexpr int kProducerThreads = 128;
 constexpr int kLaunchRegs = 168;
-constexpr int kProducerRegs = 56;
-constexpr int kConsumerRegs = 224;
-static_assert(128 * kProducerRegs + 256 * kConsumerRegs <= 384 * kLaunchRegs,
-              "register split exceeds the launch allocation");
 
-__device__ __forceinline__ void producer_regs() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-}
-__device__ __forceinline__ void consumer_regs() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-}
+template <int PRODUCER_REGS>
+struct RegSplit {
+    static constexpr int kProducer = PRODUCER_REGS;
+    // what the producer gives back, shared by the 256 consumer threads
+    static constexpr int kConsumer = ((384 * kLaunchRegs - 128 * PRODUCER_REGS) / 256) / 8 * 8;
+    static_assert(kConsumer <= 256 && PRODUCER_REGS >= 24 && PRODUCER_REGS % 8 == 0,
+                  "setmaxnreg range");
+    static_assert(128 * kProducer + 256 * kConsumer <= 384 * kLaunchRegs,
+                  "register split exceeds the launch allocation");
+    __device__ __forceinline__ static void producer() {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducer));
+    }
+    __device__ __forceinline__ static void consumer() {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumer));
+    }
+};
 
 // Byte offset of A element (r, kk) inside a stage's A tile.
 __device__ __forceinline__ uint32_t a_tile_offset(int r, int kk) {
@@ -135,12 +141,12 @@ __device__ __forceinline__ void mma_stage(Accum<Cfg> &acc, const float *As, cons
 struct TileRaster {
     int tiles_m, tiles_n;
     static constexpr int kGroupM = 8;
-    __device__ __forceinline__ void at(int64_t t, int &tm, int &tn) const {
-        const int64_t per_group = static_cast<int64_t>(kGroupM) * tiles_n;
-        const int group = static_cast<int>(t / per_group);
+    __device__ __forceinline__ void at(int t, int &tm, int &tn) const {
+        const int per_group = kGroupM * tiles_n;
+        const int group = t / per_group;
         const int first_m = group * kGroupM;
         const int gsize = min(tiles_m - first_m, kGroupM);
-        const int r = static_cast<int>(t % per_group);
+        const int r = t - group * per_group;
         tm = first_m + r % gsize;
         tn = r / gsize;
     }
