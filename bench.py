@@ -130,17 +130,19 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/dram_traffic.txt), if it was taken on the current kernel
+    sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
-        rec = json.load(open(path))
-    except (OSError, ValueError):
+        lines = open(path).read().splitlines()
+    except OSError:
         return None
-    e = rec.get(f"{kernel}:{workload}")
-    if not e or e.get("source_hash") != kernel_source_hash():
-        return None
-    return e.get("bytes_per_launch")
+    for line in lines:
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            return int(parts[3]) if parts[2] == kernel_source_hash() else None
+    return None
 
 
 class L2Flusher:
