@@ -174,6 +174,19 @@ def time_calls(fn, steps: int, warmup: int, flush, stream) -> list[float]:
     return times
 
 
+def combine_ranks(ms_local: float, flops_per_rank: float, world: int, dist=None, device="cpu"):
+    """Replicas only: every rank ran the same workload on its own GPU with no
+    exchange. Returns (the slowest rank's ms per step, whole-job GFLOP/s =
+    all ranks' flops / that time)."""
+    ms = ms_local
+    if world > 1 and dist is not None:
+        import torch
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * flops_per_rank / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
     import implicit_gemm_convolution_gb300 as om
@@ -230,13 +243,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clock_summary = clocks.summary(region0, region1)
     clocks.__exit__(None, None, None)
     ms_local = float(np.mean(kernel_ms))
-    ms = ms_local
+    ms, value = combine_ranks(ms_local, flops, world, dist, dev)
     if dist is not None:
-        t = torch.tensor([ms_local], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
-    value = world * flops / (ms * 1e-3) / 1e9  # GFLOP/s over all ranks
     achieved_tflops = flops / (ms_local * 1e-3) / 1e12
     peak_exact = fp32_peak_tflops(sms, exact=True)
 
