@@ -39,6 +39,20 @@ SM_MAX_MHZ = 2070.0
 FP32_LANES_PER_SM = 128
 
 
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates of the part
+
+
+def measured_peaks() -> dict:
+    """The measured bf16 tensor peak, else the documented fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
+                "basis": "measured bf16 burst (MEASURED_PEAKS.json)"}
+    except (OSError, ValueError, KeyError):
+        return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "basis": "fallback bf16 1.9 PFLOP/s"}
+
+
 def fp32_peak_tflops(sms: int, exact: bool) -> float:
     p = sms * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
     return p / 2 if exact else p
@@ -293,6 +307,28 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
                         "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
 
+    def tf32x3_line(name, case_):
+        Ad = torch.from_numpy(case_.A).to(dev)
+        Bd = torch.from_numpy(case_.B).to(dev)
+        Cd = torch.from_numpy(case_.C_init).to(dev)
+
+        def f():
+            st = om.gemm_raw(case_.m, case_.n, case_.k, Ad.data_ptr(), case_.lda, Bd.data_ptr(),
+                             case_.ldb, Cd.data_ptr(), case_.ldc, "tf32x3", stream)
+            if st != 0:
+                raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
+        t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
+        fl = 2.0 * case_.m * case_.n * case_.k
+        tf = fl / (t * 1e-3) / 1e12
+        peaks = measured_peaks()
+        tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+        extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
+                        "vs_fp32_fma_peak": round(tf / fp32_peak_tflops(sms, exact=False), 3),
+                        "tensor_frac": round(3 * tf / tf32_peak, 4),
+                        "tensor_peak_tflops": round(tf32_peak, 1),
+                        "tensor_peak_basis": peaks["basis"] + " x nominal tf32/bf16 ratio 1.1/2.25; "
+                                             "three tensor-core products per useful flop"}
+
     def conv_line(name, mode, c):
         x = torch.from_numpy(c.x).to(dev)
         w = torch.from_numpy(c.w).to(dev)
@@ -316,6 +352,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     if not args.headline_only:
         gemm_line("gemm_4096^3_fast", "fast", case)
+        tf32x3_line("gemm_4096^3_tf32x3", case)
         gemm_line("gemm_prefill_512x11008x4096_exact", "exact", synth.workload_gemm_prefill(False))
         gemm_line("gemm_prefill_509x11005x4096_exact", "exact", synth.workload_gemm_prefill(True))
         for md in ("exact", "fast"):

@@ -201,7 +201,11 @@ int om_gemm_f32(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, co
     if (used && (overlaps(rc, ra) || overlaps(rc, rb))) return OM_ERR_ALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc};
-    if (mode == OM_MODE_TF32X3) return OM_ERR_UNSUPPORTED;
+    if (mode == OM_MODE_TF32X3) {
+        if (k == 0) return from_cuda(om::launch_gemm_naive(p, OM_MODE_EXACT, s));  // +0
+        const cudaError_t e = om::launch_gemm_tf32x3(p, s);
+        return e == cudaErrorNotSupported ? OM_ERR_UNSUPPORTED : from_cuda(e);
+    }
     const int cfg = forced("OM_FORCE_GEMM_CFG");
     if (k == 0 || cfg == om::kCfgNaive) return from_cuda(om::launch_gemm_naive(p, mode, s));
     cudaError_t e;
@@ -265,10 +269,11 @@ int om_conv2d_f32_packed(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t C
 
 int om_device_status(void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     if (om::read_clear_status_gemm(&a, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_conv(&b, s) != cudaSuccess) return OM_ERR_CUDA;
-    return ((a | b) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
+    if (om::read_clear_status_tc(&c, s) != cudaSuccess) return OM_ERR_CUDA;
+    return ((a | b | c) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
 }
 
 }  // extern "C"

@@ -60,6 +60,11 @@ cudaError_t launch_pack_conv_weights(int64_t Cout, int64_t K, int64_t Kp, const 
 cudaError_t launch_gemm_tiled(const GemmProblem &p, int mode, int cfg, cudaStream_t s);
 cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, cudaStream_t s);
 
+// OM_MODE_TF32X3 on the tensor cores (needs 16-byte aligned A, B and lda,
+// ldb multiples of 4; cudaErrorNotSupported otherwise).
+cudaError_t launch_gemm_tf32x3(const GemmProblem &p, cudaStream_t s);
+cudaError_t read_clear_status_tc(unsigned *out, cudaStream_t s);
+
 // Read and clear the device status word of the tiled translation units
 // (synchronises s).
 cudaError_t read_clear_status_gemm(unsigned *out, cudaStream_t s);
