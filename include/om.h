@@ -109,9 +109,10 @@ OM_API int64_t om_conv_out_dim(int64_t size, int64_t ksize, int64_t stride, int6
  * Bound, for outputs whose exact-mode result is finite:
  *   |C - C_exact| <= 1e-5 * sqrt(k) * sum_p |A[i][p]| * |B[p][j]|.
  * Non-finite inputs give non-finite outputs where the exact result is
- * non-finite (the class, NaN or infinity, may differ). This mode needs A and B
- * 16-byte aligned with lda and ldb multiples of 4 (the tensor-core kernel
- * fetches them with TMA); otherwise it returns OM_ERR_UNSUPPORTED.
+ * non-finite (the class, NaN or infinity, may differ). The tensor-core
+ * kernel fetches A and B with TMA, which needs them 16-byte aligned with lda
+ * and ldb multiples of 4; other operands are computed by the fast-mode
+ * CUDA-core kernel, whose result lies inside the same bound.
  */
 OM_API int om_gemm_f32(int64_t m, int64_t n, int64_t k,
                        const float *A, int64_t lda,
