@@ -290,14 +290,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # ---- per-mode and per-workload lines (same timing rules)
     extras = {}
 
-    def gemm_line(name, mode, case_):
+    wsp = om.new_workspace(dev)
+
+    def gemm_line(name, mode, case_, use_ws=False):
         Ad = torch.from_numpy(case_.A).to(dev)
         Bd = torch.from_numpy(case_.B).to(dev)
         Cd = torch.from_numpy(case_.C_init).to(dev)
 
         def f():
             st = om.gemm_raw(case_.m, case_.n, case_.k, Ad.data_ptr(), case_.lda, Bd.data_ptr(),
-                             case_.ldb, Cd.data_ptr(), case_.ldc, mode, stream)
+                             case_.ldb, Cd.data_ptr(), case_.ldc, mode, stream,
+                             workspace=wsp if use_ws else None)
             if st != 0:
                 raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
         t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
@@ -329,7 +332,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "tensor_peak_basis": peaks["basis"] + " x nominal tf32/bf16 ratio 1.1/2.25; "
                                              "three tensor-core products per useful flop"}
 
-    def conv_line(name, mode, c):
+    def conv_line(name, mode, c, use_ws=False):
         x = torch.from_numpy(c.x).to(dev)
         w = torch.from_numpy(c.w).to(dev)
         OH = om.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.dil)
@@ -338,9 +341,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         L = om.lib()
 
         def f():
-            st = L.om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad,
-                                 c.dil, x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[mode],
-                                 stream.cuda_stream)
+            args = (c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad, c.dil,
+                    x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[mode])
+            if use_ws:
+                st = L.om_conv2d_f32_ws(*args, wsp.data_ptr(), om.workspace_bytes(),
+                                        stream.cuda_stream)
+            else:
+                st = L.om_conv2d_f32(*args, stream.cuda_stream)
             if st != 0:
                 raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
         t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
@@ -352,7 +359,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     if not args.headline_only:
         gemm_line("gemm_4096^3_fast", "fast", case)
+        gemm_line("gemm_4096^3_exact_ws", "exact", case, use_ws=True)
+        gemm_line("gemm_4096^3_fast_ws", "fast", case, use_ws=True)
         tf32x3_line("gemm_4096^3_tf32x3", case)
+        gemm_line("gemm_prefill_512x11008x4096_exact_ws", "exact",
+                  synth.workload_gemm_prefill(False), use_ws=True)
+        gemm_line("gemm_prefill_509x11005x4096_exact_ws", "exact",
+                  synth.workload_gemm_prefill(True), use_ws=True)
+        for md in ("exact", "fast"):
+            conv_line(f"conv3x3_n32_c64_56_{md}_ws", md, synth.workload_conv3x3(), use_ws=True)
+            conv_line(f"conv1x1_n32_c256to64_56_{md}_ws", md, synth.workload_conv1x1(), use_ws=True)
+        conv_line("conv_g32_s2_d2_n16_c256_28_exact_ws", "exact", synth.workload_conv_grouped(),
+                  use_ws=True)
         gemm_line("gemm_prefill_512x11008x4096_exact", "exact", synth.workload_gemm_prefill(False))
         gemm_line("gemm_prefill_509x11005x4096_exact", "exact", synth.workload_gemm_prefill(True))
         for md in ("exact", "fast"):

@@ -83,6 +83,15 @@ def lib() -> ctypes.CDLL:
             L.om_pack_conv_weights.argtypes = [i64] * 5 + [vp, vp, ctypes.POINTER(ctypes.c_size_t), vp]
             L.om_device_status.restype = ci
             L.om_device_status.argtypes = [vp]
+            L.om_workspace_bytes.restype = ctypes.c_size_t
+            L.om_gemm_f32_ws.restype = ci
+            L.om_gemm_f32_ws.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, vp,
+                                         ctypes.c_size_t, vp]
+            L.om_conv2d_f32_ws.restype = ci
+            L.om_conv2d_f32_ws.argtypes = [i64] * 11 + [vp, vp, vp, ci, vp, ctypes.c_size_t, vp]
+            L.om_conv2d_f32_packed_ws.restype = ci
+            L.om_conv2d_f32_packed_ws.argtypes = [i64] * 11 + [vp, vp, vp, ci, vp,
+                                                  ctypes.c_size_t, vp]
             _lib = L
     return _lib
 
@@ -124,13 +133,33 @@ def conv_out_dim(size: int, ksize: int, stride: int = 1, pad: int = 0, dil: int 
     return int(v)
 
 
-def gemm_raw(m, n, k, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, mode="exact", stream=None) -> int:
-    """Calls om_gemm_f32 on raw device pointers; returns the status code."""
-    return lib().om_gemm_f32(m, n, k, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, _mode(mode),
-                             _stream_handle(stream))
+def workspace_bytes() -> int:
+    """Device scratch bytes the balanced-schedule entry points need."""
+    return int(lib().om_workspace_bytes())
 
 
-def gemm(A, B, out=None, mode="exact", stream=None):
+def new_workspace(device=None):
+    """A device tensor usable as the workspace of the *_ws entry points."""
+    import torch
+    return torch.zeros((workspace_bytes() + 3) // 4, dtype=torch.int32, device=device or "cuda")
+
+
+def _ws_args(workspace):
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def gemm_raw(m, n, k, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, mode="exact", stream=None,
+             workspace=None) -> int:
+    """Calls om_gemm_f32 (om_gemm_f32_ws when a workspace tensor is given) on
+    raw device pointers; returns the status code."""
+    if workspace is None:
+        return lib().om_gemm_f32(m, n, k, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, _mode(mode),
+                                 _stream_handle(stream))
+    return lib().om_gemm_f32_ws(m, n, k, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, _mode(mode),
+                                *_ws_args(workspace), _stream_handle(stream))
+
+
+def gemm(A, B, out=None, mode="exact", stream=None, workspace=None):
     """C = A @ B (row-major views; leading dimensions from the row strides)."""
     import torch
     _require(A, "A", 2)
@@ -151,7 +180,7 @@ def gemm(A, B, out=None, mode="exact", stream=None):
     ldb = B.stride(0) if k > 1 else max(n, 1)
     ldc = out.stride(0) if m > 1 else max(n, 1)
     _check(gemm_raw(m, n, k, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, mode,
-                    stream), "om_gemm_f32")
+                    stream, workspace), "om_gemm_f32")
     return out
 
 
@@ -166,7 +195,7 @@ def _conv_geom(x, w_shape, stride, padding, dilation, groups):
 
 
 def conv2d(x, w, stride: int = 1, padding: int = 0, dilation: int = 1, groups: int = 1,
-           out=None, mode="exact", stream=None):
+           out=None, mode="exact", stream=None, workspace=None):
     """NCHW convolution without bias (implicit GEMM on the GPU)."""
     import torch
     _require(x, "x", 4)
@@ -179,8 +208,13 @@ def conv2d(x, w, stride: int = 1, padding: int = 0, dilation: int = 1, groups: i
     _require(out, "out", 4)
     if tuple(out.shape) != yshape or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor of the output shape")
-    _check(lib().om_conv2d_f32(*args, x.data_ptr(), w.data_ptr(), out.data_ptr(), _mode(mode),
-                               _stream_handle(stream)), "om_conv2d_f32")
+    if workspace is None:
+        st = lib().om_conv2d_f32(*args, x.data_ptr(), w.data_ptr(), out.data_ptr(), _mode(mode),
+                                 _stream_handle(stream))
+    else:
+        st = lib().om_conv2d_f32_ws(*args, x.data_ptr(), w.data_ptr(), out.data_ptr(), _mode(mode),
+                                    *_ws_args(workspace), _stream_handle(stream))
+    _check(st, "om_conv2d_f32")
     return out
 
 
@@ -208,7 +242,7 @@ def pack_conv_weights(w, groups: int = 1, stream=None):
 
 
 def conv2d_packed(x, w_packed, w_shape, stride: int = 1, padding: int = 0, dilation: int = 1,
-                  groups: int = 1, out=None, mode="exact", stream=None):
+                  groups: int = 1, out=None, mode="exact", stream=None, workspace=None):
     """conv2d with weights from pack_conv_weights (w_shape = the unpacked shape)."""
     import torch
     _require(x, "x", 4)
@@ -216,8 +250,14 @@ def conv2d_packed(x, w_packed, w_shape, stride: int = 1, padding: int = 0, dilat
     args, yshape = _conv_geom(x, tuple(w_shape), stride, padding, dilation, groups)
     if out is None:
         out = torch.empty(yshape, dtype=torch.float32, device=x.device)
-    _check(lib().om_conv2d_f32_packed(*args, x.data_ptr(), w_packed.data_ptr(), out.data_ptr(),
-                                      _mode(mode), _stream_handle(stream)), "om_conv2d_f32_packed")
+    if workspace is None:
+        st = lib().om_conv2d_f32_packed(*args, x.data_ptr(), w_packed.data_ptr(), out.data_ptr(),
+                                        _mode(mode), _stream_handle(stream))
+    else:
+        st = lib().om_conv2d_f32_packed_ws(*args, x.data_ptr(), w_packed.data_ptr(),
+                                           out.data_ptr(), _mode(mode), *_ws_args(workspace),
+                                           _stream_handle(stream))
+    _check(st, "om_conv2d_f32_packed")
     return out
 
 

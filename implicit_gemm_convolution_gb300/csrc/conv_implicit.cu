@@ -27,6 +27,7 @@
 #include <cstring>
 
 #include "om_internal.h"
+#include "schedule_host.h"
 #include "simt_tile.cuh"
 
 namespace om {
@@ -57,28 +58,31 @@ __device__ __forceinline__ void conv_record_timeout(int *abort_flag) {
 
 // Tile t -> (m tile, column tile, group); the m tiles of one column strip are
 // adjacent so they run together and share the gathered input through L2.
-__device__ __forceinline__ void conv_tile(const ConvGeom &g, int64_t t, int &tm, int64_t &tn,
+__device__ __forceinline__ void conv_tile(const ConvGeom &g, int t, int &tm, int64_t &tn,
                                           int &grp) {
-    tm = static_cast<int>(t % g.tiles_m);
-    const int64_t r = t / g.tiles_m;
+    tm = t % g.tiles_m;
+    const int r = t / g.tiles_m;
     tn = r % g.tiles_n;
-    grp = static_cast<int>(r / g.tiles_n);
+    grp = r / g.tiles_n;
 }
 
 template <class Cfg, bool A_TMA>
 __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMap *mapW,
                                              uint8_t *smem, uint64_t *full, uint64_t *empty,
-                                             int *abort_flag, int64_t total, int nk, int pt) {
+                                             int *abort_flag, const Schedule &sched, int pt) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
     constexpr int CPT = BN / kProducerThreads;  // gathered columns per producer thread
     static_assert(BN % kProducerThreads == 0, "columns split evenly over the producer");
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    const int taps_per_channel = g.KH * g.KW;
+    const Schedule::Local L = sched.local();
+    for (int si = 0; si < L.count; ++si) {
+        const Segment sg = sched.at(L, si);
         int tm, grp;
         int64_t tn;
-        conv_tile(g, t, tm, tn, grp);
+        conv_tile(g, sg.tile, tm, tn, grp);
         // Per gathered column: the group's first input plane of its image and
         // the input coordinates of tap (0, 0).
         const float *base[CPT];
@@ -96,9 +100,12 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
             ix0[j] = ox * g.sW - g.pL;
         }
         const int row0 = grp * g.M + tm * BM;  // first weight row of the tile
-        // tap state of the first tap of the stage: p = (c*KH + ky)*KW + kx
-        int c = 0, ky = 0, kx = 0;
-        for (int kt = 0; kt < nk; ++kt) {
+        // tap state of the segment's first tap p = (c*KH + ky)*KW + kx
+        const int p0 = sg.kb * BK;
+        int c = p0 / taps_per_channel;
+        int ky = (p0 - c * taps_per_channel) / g.KW;
+        int kx = p0 - c * taps_per_channel - ky * g.KW;
+        for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
                 conv_record_timeout(abort_flag);
                 cp_async_wait_all();
@@ -166,9 +173,67 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
     cp_async_wait_all();
 }
 
+// Moves this thread's outputs of a tile between registers and y. Row i of
+// the tile is output channel grp*M + tm*BM + i; column j is (image, pixel) =
+// divmod(j, OH*OW). OP 0: final store (canonical NaN); 1: raw store of an
+// early part's accumulators; 2: load of the accumulators an earlier CTA stored.
+template <class Cfg, int OP>
+__device__ __forceinline__ void conv_tile_io(const ConvGeom &g, Accum<Cfg> &acc, int tm,
+                                             int64_t tn, int grp, int arow0, int bcol0) {
+    const bool vec_ok = (g.P % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.y) & 15) == 0);
+#pragma unroll
+    for (int q = 0; q < Cfg::TN / 4; ++q) {
+        const int64_t col = tn * Cfg::BN + bcol0 + 16 * q;
+        if (col >= g.ncols) continue;
+        const int64_t img = col / g.P;
+        const int pix = static_cast<int>(col - img * g.P);
+        const bool vec = vec_ok && (col + 3 < g.ncols);
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i) {
+            const int mrow = tm * Cfg::BM + arow0 + 8 * i;
+            if (mrow >= g.M) continue;
+            const int oc = grp * g.M + mrow;
+            float *dst = g.y + (img * g.Cout + oc) * static_cast<int64_t>(g.P) + pix;
+            if constexpr (OP == 2) {
+                float e[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (vec) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(dst));
+                    e[0] = v.x; e[1] = v.y; e[2] = v.z; e[3] = v.w;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int64_t cu = col + u;
+                        if (cu >= g.ncols) break;
+                        const int64_t iu = cu / g.P;
+                        e[u] = __ldcg(g.y + (iu * g.Cout + oc) * static_cast<int64_t>(g.P) + (cu - iu * g.P));
+                    }
+                }
+                acc.v[i][2 * q] = make_float2(e[0], e[1]);
+                acc.v[i][2 * q + 1] = make_float2(e[2], e[3]);
+            } else {
+                const float4 v = (OP == 0) ? acc.out4(i, q)
+                                           : make_float4(acc.v[i][2 * q].x, acc.v[i][2 * q].y,
+                                                         acc.v[i][2 * q + 1].x, acc.v[i][2 * q + 1].y);
+                if (vec) {
+                    *reinterpret_cast<float4 *>(dst) = v;
+                } else {
+                    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int64_t cu = col + u;
+                        if (cu >= g.ncols) break;
+                        const int64_t iu = cu / g.P;
+                        g.y[(iu * g.Cout + oc) * static_cast<int64_t>(g.P) + (cu - iu * g.P)] = e[u];
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <int MODE, class Cfg, bool A_TMA>
 __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
-    conv_implicit_kernel(const __grid_constant__ CUtensorMap mapW, ConvGeom g) {
+    conv_implicit_kernel(const __grid_constant__ CUtensorMap mapW, ConvGeom g, Schedule sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = aligned_smem<Cfg>(smem_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
@@ -188,15 +253,12 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     }
     __syncthreads();
 
-    const int64_t total = static_cast<int64_t>(g.tiles_m) * g.tiles_n * g.G;
-    const int nk = (g.K + Cfg::BK - 1) / Cfg::BK;
-
     if (warp >= Cfg::CONSUMER_WARPS) {
         RegSplit<CONV_PRODUCER_REGS>::producer();
         if constexpr (A_TMA) {
             if (threadIdx.x == Cfg::CONSUMERS) prefetch_tensormap(&mapW);
         }
-        conv_produce<Cfg, A_TMA>(g, &mapW, smem, full, empty, abort_flag, total, nk,
+        conv_produce<Cfg, A_TMA>(g, &mapW, smem, full, empty, abort_flag, sched,
                                  threadIdx.x - Cfg::CONSUMERS);
         return;
     }
@@ -205,16 +267,24 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     const int ty = lane / 4, tx = lane % 4;
     const int arow0 = (warp / Cfg::WARPS_N) * Cfg::WM + ty;
     const int bcol0 = (warp % Cfg::WARPS_N) * Cfg::WN + tx * 4;
-    const bool vec_ok = (g.P % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.y) & 15) == 0);
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    const Schedule::Local L = sched.local();
+    for (int si = 0; si < L.count; ++si) {
+        const Segment sg = sched.at(L, si);
         int tm, grp;
         int64_t tn;
-        conv_tile(g, t, tm, tn, grp);
+        conv_tile(g, sg.tile, tm, tn, grp);
         Accum<Cfg> acc;
         acc.zero();
-        for (int kt = 0; kt < nk; ++kt) {
+        if (sg.kind == kSegLate) {
+            if (!wait_previous_part(sched.flags, Cfg::CONSUMERS, abort_flag)) {
+                atomicOr(&g_status_conv, kDevErrTimeout);
+                return;
+            }
+            conv_tile_io<Cfg, 2>(g, acc, tm, tn, grp, arow0, bcol0);
+        }
+        for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&full[stage], phase)) {
                 conv_record_timeout(abort_flag);
                 return;
@@ -229,36 +299,11 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
                 phase ^= 1;
             }
         }
-        // Epilogue: row i of the tile is output channel grp*M + tm*BM + i,
-        // column j is (image, pixel) = divmod(j, OH*OW).
-#pragma unroll
-        for (int q = 0; q < Cfg::TN / 4; ++q) {
-            const int64_t col = tn * Cfg::BN + bcol0 + 16 * q;
-            if (col >= g.ncols) continue;
-            const int64_t img = col / g.P;
-            const int pix = static_cast<int>(col - img * g.P);
-            const bool vec = vec_ok && (col + 3 < g.ncols);
-#pragma unroll
-            for (int i = 0; i < Cfg::TM; ++i) {
-                const int mrow = tm * Cfg::BM + arow0 + 8 * i;
-                if (mrow >= g.M) continue;
-                const int oc = grp * g.M + mrow;
-                const float4 v = acc.out4(i, q);
-                float *dst = g.y + (img * g.Cout + oc) * static_cast<int64_t>(g.P) + pix;
-                if (vec) {
-                    *reinterpret_cast<float4 *>(dst) = v;
-                } else {
-                    const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int64_t cu = col + u;
-                        if (cu >= g.ncols) break;
-                        const int64_t iu = cu / g.P;
-                        const int64_t pu = cu - iu * g.P;
-                        g.y[(iu * g.Cout + oc) * static_cast<int64_t>(g.P) + pu] = e[u];
-                    }
-                }
-            }
+        if (sg.kind == kSegEarly) {
+            conv_tile_io<Cfg, 1>(g, acc, tm, tn, grp, arow0, bcol0);
+            signal_early_part(sched.flags, Cfg::CONSUMERS);
+        } else {
+            conv_tile_io<Cfg, 0>(g, acc, tm, tn, grp, arow0, bcol0);
         }
     }
 }
@@ -295,7 +340,7 @@ static bool make_weight_map(CUtensorMap *map, const ConvProblem &p, int box_rows
 using ConvCfg64x256 = TileCfg<64, 256, 8, 8, 1, 8, 4, true>;
 
 template <int MODE, class Cfg>
-static cudaError_t launch_conv_cfg(const ConvProblem &p, cudaStream_t s) {
+static cudaError_t launch_conv_cfg(const ConvProblem &p, unsigned *flags, cudaStream_t s) {
     ConvGeom g;
     g.x = p.x; g.w = p.w; g.y = p.y;
     g.ncols = p.N * p.OH * p.OW;
@@ -311,36 +356,32 @@ static cudaError_t launch_conv_cfg(const ConvProblem &p, cudaStream_t s) {
     g.G = static_cast<int>(p.G);
     const int64_t tiles_m = (g.M + Cfg::BM - 1) / Cfg::BM;
     const int64_t tiles_n = (g.ncols + Cfg::BN - 1) / Cfg::BN;
-    if (tiles_n > 0x7FFFFFFF || p.w_ld > 0x7FFFFFFF) return cudaErrorNotSupported;
+    if (tiles_m * tiles_n * p.G > 0x7FFFFFFF || p.w_ld > 0x7FFFFFFF) return cudaErrorNotSupported;
     g.tiles_m = static_cast<int>(tiles_m);
     g.tiles_n = static_cast<int>(tiles_n);
-    const int64_t total = tiles_m * tiles_n * p.G;
-    const int64_t grid = total < num_sms() ? total : num_sms();
+    Schedule sched;
+    make_schedule(static_cast<int>(tiles_m * tiles_n * p.G), (g.K + Cfg::BK - 1) / Cfg::BK, flags,
+                  &sched);
 
     CUtensorMap map;
     memset(&map, 0, sizeof(map));
     const bool a_tma = ((reinterpret_cast<uintptr_t>(p.w) & 15) == 0) && (p.w_ld % 4 == 0) &&
                        make_weight_map(&map, p, Cfg::BM);
-    cudaError_t e;
-    if (a_tma) {
-        auto kernel = conv_implicit_kernel<MODE, Cfg, true>;
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        kernel<<<static_cast<unsigned>(grid), Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s>>>(map, g);
-    } else {
-        auto kernel = conv_implicit_kernel<MODE, Cfg, false>;
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        kernel<<<static_cast<unsigned>(grid), Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s>>>(map, g);
-    }
-    return cudaGetLastError();
+    void (*kernel)(const CUtensorMap, ConvGeom, Schedule) =
+        a_tma ? conv_implicit_kernel<MODE, Cfg, true> : conv_implicit_kernel<MODE, Cfg, false>;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s,
+                            map, g, sched);
 }
 
-cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, cudaStream_t s) {
+cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, unsigned *flags,
+                                 cudaStream_t s) {
     if (cfg != kConvAuto && cfg != kConvImplicit) return cudaErrorNotSupported;
     if (p.K == 0) return cudaErrorNotSupported;
-    return mode == kFast ? launch_conv_cfg<kFast, ConvCfg64x256>(p, s)
-                         : launch_conv_cfg<kExact, ConvCfg64x256>(p, s);
+    return mode == kFast ? launch_conv_cfg<kFast, ConvCfg64x256>(p, flags, s)
+                         : launch_conv_cfg<kExact, ConvCfg64x256>(p, flags, s);
 }
 
 cudaError_t read_clear_status_conv(unsigned *out, cudaStream_t s) {

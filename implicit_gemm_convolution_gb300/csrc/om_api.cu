@@ -133,11 +133,13 @@ int validate_conv(const ConvArgs &a, const float *x, const float *w, bool packed
     return OM_OK;
 }
 
-// Output tiles are handed to a persistent grid of one CTA per SM, so a
-// launch costs whole rounds of tiles. Pick the tile shape with the smaller
-// number of rounds times tile size (ties go to the larger tile, which reuses
-// each operand load over more outputs).
-int pick_gemm_cfg(const GemmProblem &p) {
+// Output tiles are handed to a persistent grid of one CTA per SM. Without a
+// workspace a launch costs whole rounds of tiles, so pick the tile shape with
+// the fewer rounds times tile size (ties go to the larger tile, which reuses
+// each operand load over more outputs). With a workspace the last rounds are
+// balanced across the SMs and the larger tile is always taken.
+int pick_gemm_cfg(const GemmProblem &p, bool balanced) {
+    if (balanced) return om::kCfgTma128x256;
     const int64_t sms = om::num_sms();
     const int64_t tm = (p.m + 127) / 128;
     const int64_t t256 = tm * ((p.n + 255) / 256), t128 = tm * ((p.n + 127) / 128);
@@ -146,12 +148,87 @@ int pick_gemm_cfg(const GemmProblem &p) {
     return c128 < c256 ? om::kCfgTma128x128 : om::kCfgTma128x256;
 }
 
-int run_conv(const ConvProblem &p, int mode, cudaStream_t s) {
-    int cfg = forced("OM_FORCE_CONV_CFG");
+int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
+    const int cfg = forced("OM_FORCE_CONV_CFG");
     if (cfg == om::kConvNaive || p.K == 0) return from_cuda(om::launch_conv_naive(p, mode, s));
-    cudaError_t e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, s);
+    cudaError_t e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
     return from_cuda(e);
+}
+
+// Validates a caller workspace; *flags stays NULL when none was given.
+int check_workspace(void *ws, size_t bytes, unsigned **flags) {
+    *flags = nullptr;
+    if (!ws) return OM_OK;
+    if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return OM_ERR_ALIGNMENT;
+    if (bytes < static_cast<size_t>(om::kMaxScheduleCtas) * sizeof(unsigned)) return OM_ERR_INVALID_ARG;
+    *flags = static_cast<unsigned *>(ws);
+    return OM_OK;
+}
+
+Range ws_range(const unsigned *flags) { return span(flags, flags ? om::kMaxScheduleCtas : 0); }
+
+int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, const float *B,
+              int64_t ldb, float *C, int64_t ldc, int mode, void *workspace, size_t ws_bytes,
+              void *stream) {
+    if (m < 0 || n < 0 || k < 0) return OM_ERR_INVALID_ARG;
+    if (mode != OM_MODE_EXACT && mode != OM_MODE_FAST && mode != OM_MODE_TF32X3)
+        return OM_ERR_UNSUPPORTED;
+    unsigned *flags = nullptr;
+    const int wst = check_workspace(workspace, ws_bytes, &flags);
+    if (wst != OM_OK) return wst;
+    if (m == 0 || n == 0) return OM_OK;
+    const bool used = k > 0;
+    if (used && (lda < k || ldb < n)) return OM_ERR_INVALID_ARG;
+    if (ldc < n) return OM_ERR_INVALID_ARG;
+    if (!C || (used && (!A || !B))) return OM_ERR_NULL_PTR;
+    if (!aligned4(C) || (used && (!aligned4(A) || !aligned4(B)))) return OM_ERR_ALIGNMENT;
+    Range rc, ra, rb;
+    if (!block_range(C, m, n, ldc, &rc)) return OM_ERR_TOO_LARGE;
+    if (used && !block_range(A, m, k, lda, &ra)) return OM_ERR_TOO_LARGE;
+    if (used && !block_range(B, k, n, ldb, &rb)) return OM_ERR_TOO_LARGE;
+    if (used && (overlaps(rc, ra) || overlaps(rc, rb))) return OM_ERR_ALIAS;
+    const Range rw = ws_range(flags);
+    if (flags && (overlaps(rw, rc) || (used && (overlaps(rw, ra) || overlaps(rw, rb)))))
+        return OM_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc};
+    if (mode == OM_MODE_TF32X3) {
+        if (k == 0) return from_cuda(om::launch_gemm_naive(p, OM_MODE_EXACT, s));  // +0
+        cudaError_t e = om::launch_gemm_tf32x3(p, s);
+        // Operands TMA cannot fetch take the fast-mode CUDA-core kernel: one
+        // correctly rounded fused multiply-add per term is well inside the
+        // tolerance mode's bound.
+        if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, OM_MODE_FAST, om::kCfgAsync128x128, flags, s);
+        if (e == cudaErrorNotSupported) e = om::launch_gemm_naive(p, OM_MODE_FAST, s);
+        return from_cuda(e);
+    }
+    int cfg = forced("OM_FORCE_GEMM_CFG");
+    if (k == 0 || cfg == om::kCfgNaive) return from_cuda(om::launch_gemm_naive(p, mode, s));
+    if (cfg < 0) cfg = pick_gemm_cfg(p, flags != nullptr);
+    cudaError_t e = om::launch_gemm_tiled(p, mode, cfg, flags, s);
+    if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, mode, om::kCfgAsync128x128, flags, s);
+    if (e == cudaErrorNotSupported) e = om::launch_gemm_naive(p, mode, s);
+    return from_cuda(e);
+}
+
+int conv_impl(const ConvArgs &a, const float *x, const float *w, bool packed, float *y, int mode,
+              void *workspace, size_t ws_bytes, void *stream) {
+    unsigned *flags = nullptr;
+    const int wst = check_workspace(workspace, ws_bytes, &flags);
+    if (wst != OM_OK) return wst;
+    ConvProblem p;
+    bool empty = false;
+    const int st = validate_conv(a, x, w, packed, y, mode, &p, &empty);
+    if (st != OM_OK || empty) return st;
+    if (flags) {
+        const Range rw = ws_range(flags);
+        const Range ry = span(y, static_cast<__int128>(p.N) * p.Cout * p.OH * p.OW);
+        const Range rx = span(x, static_cast<__int128>(p.N) * p.Cin * p.H * p.W);
+        const Range rwt = span(w, static_cast<__int128>(p.Cout) * p.w_ld);
+        if (overlaps(rw, ry) || overlaps(rw, rx) || overlaps(rw, rwt)) return OM_ERR_ALIAS;
+    }
+    return run_conv(p, mode, flags, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -183,56 +260,36 @@ int64_t om_conv_out_dim(int64_t size, int64_t ksize, int64_t stride, int64_t pad
     return out_dim(size, ksize, stride, pad, dil);
 }
 
+size_t om_workspace_bytes(void) {
+    return static_cast<size_t>(om::kMaxScheduleCtas) * sizeof(unsigned);
+}
+
 int om_gemm_f32(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, const float *B,
                 int64_t ldb, float *C, int64_t ldc, int mode, void *stream) {
-    if (m < 0 || n < 0 || k < 0) return OM_ERR_INVALID_ARG;
-    if (mode != OM_MODE_EXACT && mode != OM_MODE_FAST && mode != OM_MODE_TF32X3)
-        return OM_ERR_UNSUPPORTED;
-    if (m == 0 || n == 0) return OM_OK;
-    const bool used = k > 0;
-    if (used && (lda < k || ldb < n)) return OM_ERR_INVALID_ARG;
-    if (ldc < n) return OM_ERR_INVALID_ARG;
-    if (!C || (used && (!A || !B))) return OM_ERR_NULL_PTR;
-    if (!aligned4(C) || (used && (!aligned4(A) || !aligned4(B)))) return OM_ERR_ALIGNMENT;
-    Range rc, ra, rb;
-    if (!block_range(C, m, n, ldc, &rc)) return OM_ERR_TOO_LARGE;
-    if (used && !block_range(A, m, k, lda, &ra)) return OM_ERR_TOO_LARGE;
-    if (used && !block_range(B, k, n, ldb, &rb)) return OM_ERR_TOO_LARGE;
-    if (used && (overlaps(rc, ra) || overlaps(rc, rb))) return OM_ERR_ALIAS;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc};
-    if (mode == OM_MODE_TF32X3) {
-        if (k == 0) return from_cuda(om::launch_gemm_naive(p, OM_MODE_EXACT, s));  // +0
-        cudaError_t e = om::launch_gemm_tf32x3(p, s);
-        // Operands TMA cannot fetch take the fast-mode CUDA-core kernel: one
-        // correctly rounded fused multiply-add per term is well inside the
-        // tolerance mode's bound.
-        if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, OM_MODE_FAST, om::kCfgAsync128x128, s);
-        if (e == cudaErrorNotSupported) e = om::launch_gemm_naive(p, OM_MODE_FAST, s);
-        return from_cuda(e);
-    }
-    const int cfg = forced("OM_FORCE_GEMM_CFG");
-    if (k == 0 || cfg == om::kCfgNaive) return from_cuda(om::launch_gemm_naive(p, mode, s));
-    cudaError_t e;
-    if (cfg > 0) {
-        e = om::launch_gemm_tiled(p, mode, cfg, s);
-    } else {
-        e = om::launch_gemm_tiled(p, mode, pick_gemm_cfg(p), s);
-        if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, mode, om::kCfgAsync128x128, s);
-    }
-    if (e == cudaErrorNotSupported) e = om::launch_gemm_naive(p, mode, s);
-    return from_cuda(e);
+    return gemm_impl(m, n, k, A, lda, B, ldb, C, ldc, mode, nullptr, 0, stream);
+}
+
+int om_gemm_f32_ws(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, const float *B,
+                   int64_t ldb, float *C, int64_t ldc, int mode, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+    if (!workspace) return OM_ERR_NULL_PTR;
+    return gemm_impl(m, n, k, A, lda, B, ldb, C, ldc, mode, workspace, workspace_bytes, stream);
 }
 
 int om_conv2d_f32(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout, int64_t G,
                   int64_t KH, int64_t KW, int64_t stride, int64_t pad, int64_t dil,
                   const float *x, const float *w, float *y, int mode, void *stream) {
     const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
-    ConvProblem p;
-    bool empty = false;
-    const int st = validate_conv(a, x, w, false, y, mode, &p, &empty);
-    if (st != OM_OK || empty) return st;
-    return run_conv(p, mode, static_cast<cudaStream_t>(stream));
+    return conv_impl(a, x, w, false, y, mode, nullptr, 0, stream);
+}
+
+int om_conv2d_f32_ws(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout, int64_t G,
+                     int64_t KH, int64_t KW, int64_t stride, int64_t pad, int64_t dil,
+                     const float *x, const float *w, float *y, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    if (!workspace) return OM_ERR_NULL_PTR;
+    const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
+    return conv_impl(a, x, w, false, y, mode, workspace, workspace_bytes, stream);
 }
 
 int om_pack_conv_weights(int64_t Cout, int64_t Cin, int64_t G, int64_t KH, int64_t KW,
@@ -265,11 +322,16 @@ int om_conv2d_f32_packed(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t C
                          const float *x, const float *w_packed, float *y, int mode,
                          void *stream) {
     const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
-    ConvProblem p;
-    bool empty = false;
-    const int st = validate_conv(a, x, w_packed, true, y, mode, &p, &empty);
-    if (st != OM_OK || empty) return st;
-    return run_conv(p, mode, static_cast<cudaStream_t>(stream));
+    return conv_impl(a, x, w_packed, true, y, mode, nullptr, 0, stream);
+}
+
+int om_conv2d_f32_packed_ws(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout, int64_t G,
+                            int64_t KH, int64_t KW, int64_t stride, int64_t pad, int64_t dil,
+                            const float *x, const float *w_packed, float *y, int mode,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace) return OM_ERR_NULL_PTR;
+    const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
+    return conv_impl(a, x, w_packed, true, y, mode, workspace, workspace_bytes, stream);
 }
 
 int om_device_status(void *stream) {

@@ -57,8 +57,12 @@ cudaError_t launch_pack_conv_weights(int64_t Cout, int64_t K, int64_t Kp, const 
 
 // Tiled kernels. Return cudaErrorNotSupported when the configuration cannot
 // run this problem (the dispatcher then picks another one).
-cudaError_t launch_gemm_tiled(const GemmProblem &p, int mode, int cfg, cudaStream_t s);
-cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, cudaStream_t s);
+// flags: NULL for whole tiles only, or kMaxScheduleCtas words of caller
+// scratch for the balanced schedule with k-block continuation.
+cudaError_t launch_gemm_tiled(const GemmProblem &p, int mode, int cfg, unsigned *flags,
+                              cudaStream_t s);
+cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, unsigned *flags,
+                                 cudaStream_t s);
 
 // OM_MODE_TF32X3 on the tensor cores (needs 16-byte aligned A, B and lda,
 // ldb multiples of 4; cudaErrorNotSupported otherwise).
@@ -71,6 +75,9 @@ cudaError_t read_clear_status_gemm(unsigned *out, cudaStream_t s);
 cudaError_t read_clear_status_conv(unsigned *out, cudaStream_t s);
 
 int num_sms();
+
+// Largest grid the balanced schedule runs (one flag word per CTA).
+constexpr int kMaxScheduleCtas = 1024;
 
 // Bit of the device status words set by a bounded wait that ran out.
 constexpr unsigned kDevErrTimeoutHost = 1u;

@@ -30,6 +30,7 @@
 #include <cstring>
 
 #include "om_internal.h"
+#include "schedule_host.h"
 #include "simt_tile.cuh"
 
 namespace om {
@@ -47,15 +48,17 @@ __device__ __forceinline__ void record_timeout(int *abort_flag) {
 template <class Cfg>
 __device__ __forceinline__ void produce_tma(const CUtensorMap *mapA, const CUtensorMap *mapB,
                                             uint8_t *smem, uint64_t *full, uint64_t *empty,
-                                            int *abort_flag, const TileRaster &rs, int total,
-                                            int nk) {
+                                            int *abort_flag, const TileRaster &rs,
+                                            const Schedule &sched) {
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const Schedule::Local L = sched.local();
+    for (int i = 0; i < L.count; ++i) {
+        const Segment sg = sched.at(L, i);
         int tm, tn;
-        rs.at(t, tm, tn);
-        for (int kt = 0; kt < nk; ++kt) {
+        rs.at(sg.tile, tm, tn);
+        for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
                 record_timeout(abort_flag);
                 // Let the copies already issued land before shared memory goes away.
@@ -87,18 +90,19 @@ __device__ __forceinline__ void produce_tma(const CUtensorMap *mapA, const CUten
 template <class Cfg>
 __device__ __forceinline__ void produce_async(const GemmProblem &p, uint8_t *smem,
                                               uint64_t *full, uint64_t *empty, int *abort_flag,
-                                              const TileRaster &rs, int total, int nk,
-                                              int pt) {
+                                              const TileRaster &rs, const Schedule &sched, int pt) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
     int stage = 0;
     uint32_t phase = 0;
     const int kk_a = pt % 32;
     const int r_a0 = pt / 32;  // 0..3
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const Schedule::Local L = sched.local();
+    for (int i = 0; i < L.count; ++i) {
+        const Segment sg = sched.at(L, i);
         int tm, tn;
-        rs.at(t, tm, tn);
+        rs.at(sg.tile, tm, tn);
         const int64_t m0 = static_cast<int64_t>(tm) * BM, n0 = static_cast<int64_t>(tn) * BN;
-        for (int kt = 0; kt < nk; ++kt) {
+        for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
                 record_timeout(abort_flag);
                 cp_async_wait_all();
@@ -135,12 +139,56 @@ __device__ __forceinline__ void produce_async(const GemmProblem &p, uint8_t *sme
     cp_async_wait_all();
 }
 
+// Moves this thread's outputs of a tile between registers and C.
+// OP 0: final store (canonical NaN); 1: raw store of an early part's
+// accumulators; 2: load of the accumulators an earlier CTA stored.
+template <class Cfg, int OP>
+__device__ __forceinline__ void tile_io(const GemmProblem &p, Accum<Cfg> &acc, int64_t row0,
+                                        int64_t col0, int vec_store) {
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i) {
+        const int64_t row = row0 + 8 * i;
+        if (row >= p.m) continue;
+        float *crow = p.C + row * p.ldc;
+#pragma unroll
+        for (int q = 0; q < Cfg::TN / 4; ++q) {
+            const int64_t col = col0 + 16 * q;
+            const bool vec = vec_store && col + 3 < p.n;
+            if constexpr (OP == 2) {
+                float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (vec) {
+                    v = __ldcg(reinterpret_cast<const float4 *>(crow + col));
+                } else {
+                    if (col < p.n) v.x = __ldcg(crow + col);
+                    if (col + 1 < p.n) v.y = __ldcg(crow + col + 1);
+                    if (col + 2 < p.n) v.z = __ldcg(crow + col + 2);
+                    if (col + 3 < p.n) v.w = __ldcg(crow + col + 3);
+                }
+                acc.v[i][2 * q] = make_float2(v.x, v.y);
+                acc.v[i][2 * q + 1] = make_float2(v.z, v.w);
+            } else {
+                const float4 v = (OP == 0) ? acc.out4(i, q)
+                                           : make_float4(acc.v[i][2 * q].x, acc.v[i][2 * q].y,
+                                                         acc.v[i][2 * q + 1].x, acc.v[i][2 * q + 1].y);
+                if (vec) {
+                    *reinterpret_cast<float4 *>(crow + col) = v;
+                } else {
+                    if (col < p.n) crow[col] = v.x;
+                    if (col + 1 < p.n) crow[col + 1] = v.y;
+                    if (col + 2 < p.n) crow[col + 2] = v.z;
+                    if (col + 3 < p.n) crow[col + 3] = v.w;
+                }
+            }
+        }
+    }
+}
+
 // -------------------------------------------------------------- kernel
 template <int MODE, class Cfg, int PROD>
 __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     sgemm_tiled_kernel(const __grid_constant__ CUtensorMap mapA,
                        const __grid_constant__ CUtensorMap mapB, GemmProblem p, TileRaster rs,
-                       int vec_store) {
+                       Schedule sched, int vec_store) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = aligned_smem<Cfg>(smem_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
@@ -159,19 +207,16 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     }
     __syncthreads();
 
-    const int total = rs.tiles_m * rs.tiles_n;
-    const int nk = static_cast<int>((p.k + Cfg::BK - 1) / Cfg::BK);
-
     if (warp >= Cfg::CONSUMER_WARPS) {
         RegSplit<(PROD == kProdTma ? 24 : 56)>::producer();
         if constexpr (PROD == kProdTma) {
             if (warp == Cfg::CONSUMER_WARPS && lane == 0) {
                 prefetch_tensormap(&mapA);
                 prefetch_tensormap(&mapB);
-                produce_tma<Cfg>(&mapA, &mapB, smem, full, empty, abort_flag, rs, total, nk);
+                produce_tma<Cfg>(&mapA, &mapB, smem, full, empty, abort_flag, rs, sched);
             }
         } else {
-            produce_async<Cfg>(p, smem, full, empty, abort_flag, rs, total, nk,
+            produce_async<Cfg>(p, smem, full, empty, abort_flag, rs, sched,
                                threadIdx.x - Cfg::CONSUMERS);
         }
         return;
@@ -184,12 +229,23 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     const int bcol0 = (warp % Cfg::WARPS_N) * Cfg::WN + tx * 4;
     int stage = 0;
     uint32_t phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const Schedule::Local L = sched.local();
+    for (int si = 0; si < L.count; ++si) {
+        const Segment sg = sched.at(L, si);
         int tm, tn;
-        rs.at(t, tm, tn);
+        rs.at(sg.tile, tm, tn);
+        const int64_t row0 = static_cast<int64_t>(tm) * Cfg::BM + arow0;
+        const int64_t col0 = static_cast<int64_t>(tn) * Cfg::BN + bcol0;
         Accum<Cfg> acc;
         acc.zero();
-        for (int kt = 0; kt < nk; ++kt) {
+        if (sg.kind == kSegLate) {
+            if (!wait_previous_part(sched.flags, Cfg::CONSUMERS, abort_flag)) {
+                atomicOr(&g_status_gemm, kDevErrTimeout);
+                return;
+            }
+            tile_io<Cfg, 2>(p, acc, row0, col0, vec_store);
+        }
+        for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&full[stage], phase)) {
                 record_timeout(abort_flag);
                 return;
@@ -204,28 +260,12 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
                 phase ^= 1;
             }
         }
-
-        // Epilogue: canonical NaN, predicated stores; columns >= n untouched.
-        const int64_t row0 = static_cast<int64_t>(tm) * Cfg::BM + arow0;
-        const int64_t col0 = static_cast<int64_t>(tn) * Cfg::BN + bcol0;
-#pragma unroll
-        for (int i = 0; i < Cfg::TM; ++i) {
-            const int64_t row = row0 + 8 * i;
-            if (row >= p.m) continue;
-            float *crow = p.C + row * p.ldc;
-#pragma unroll
-            for (int q = 0; q < Cfg::TN / 4; ++q) {
-                const int64_t col = col0 + 16 * q;
-                const float4 v = acc.out4(i, q);
-                if (vec_store && col + 3 < p.n) {
-                    *reinterpret_cast<float4 *>(crow + col) = v;
-                } else {
-                    if (col < p.n) crow[col] = v.x;
-                    if (col + 1 < p.n) crow[col + 1] = v.y;
-                    if (col + 2 < p.n) crow[col + 2] = v.z;
-                    if (col + 3 < p.n) crow[col + 3] = v.w;
-                }
-            }
+        if (sg.kind == kSegEarly) {
+            tile_io<Cfg, 1>(p, acc, row0, col0, vec_store);
+            signal_early_part(sched.flags, Cfg::CONSUMERS);
+        } else {
+            // canonical NaN, predicated stores; columns >= n untouched
+            tile_io<Cfg, 0>(p, acc, row0, col0, vec_store);
         }
     }
 }
@@ -272,7 +312,7 @@ static bool tma_eligible(const GemmProblem &p) {
 }
 
 template <int MODE, class Cfg, int PROD>
-static cudaError_t launch_cfg(const GemmProblem &p, cudaStream_t s) {
+static cudaError_t launch_cfg(const GemmProblem &p, unsigned *flags, cudaStream_t s) {
     auto kernel = sgemm_tiled_kernel<MODE, Cfg, PROD>;
     CUtensorMap mapA, mapB;
     memset(&mapA, 0, sizeof(mapA));
@@ -290,12 +330,12 @@ static cudaError_t launch_cfg(const GemmProblem &p, cudaStream_t s) {
     TileRaster rs;
     rs.tiles_m = static_cast<int>(tm);
     rs.tiles_n = static_cast<int>(tn);
-    const int64_t total = tm * tn;
-    const int64_t grid = total < num_sms() ? total : num_sms();
+    Schedule sched;
+    make_schedule(static_cast<int>(tm * tn), static_cast<int>((p.k + Cfg::BK - 1) / Cfg::BK),
+                  flags, &sched);
     const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) && (p.ldc % 4 == 0);
-    kernel<<<static_cast<unsigned>(grid), Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES,
-             s>>>(mapA, mapB, p, rs, vec);
-    return cudaGetLastError();
+    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s,
+                            mapA, mapB, p, rs, sched, vec);
 }
 
 using Cfg128x256 = TileCfg<128, 256, 8, 16, 2, 4, 4, true>;
@@ -303,18 +343,20 @@ using Cfg128x128 = TileCfg<128, 128, 8, 8, 2, 4, 4, true>;
 using Cfg128x256Scalar = TileCfg<128, 256, 8, 16, 2, 4, 4, false>;
 
 template <int MODE>
-static cudaError_t launch_mode(const GemmProblem &p, int cfg, cudaStream_t s) {
+static cudaError_t launch_mode(const GemmProblem &p, int cfg, unsigned *flags, cudaStream_t s) {
     switch (cfg) {
-        case kCfgTma128x256: return launch_cfg<MODE, Cfg128x256, kProdTma>(p, s);
-        case kCfgTma128x128: return launch_cfg<MODE, Cfg128x128, kProdTma>(p, s);
-        case kCfgAsync128x128: return launch_cfg<MODE, Cfg128x128, kProdAsync>(p, s);
-        case kCfgTmaScalar128x256: return launch_cfg<MODE, Cfg128x256Scalar, kProdTma>(p, s);
+        case kCfgTma128x256: return launch_cfg<MODE, Cfg128x256, kProdTma>(p, flags, s);
+        case kCfgTma128x128: return launch_cfg<MODE, Cfg128x128, kProdTma>(p, flags, s);
+        case kCfgAsync128x128: return launch_cfg<MODE, Cfg128x128, kProdAsync>(p, flags, s);
+        case kCfgTmaScalar128x256: return launch_cfg<MODE, Cfg128x256Scalar, kProdTma>(p, flags, s);
         default: return cudaErrorNotSupported;
     }
 }
 
-cudaError_t launch_gemm_tiled(const GemmProblem &p, int mode, int cfg, cudaStream_t s) {
-    return mode == kFast ? launch_mode<kFast>(p, cfg, s) : launch_mode<kExact>(p, cfg, s);
+cudaError_t launch_gemm_tiled(const GemmProblem &p, int mode, int cfg, unsigned *flags,
+                              cudaStream_t s) {
+    return mode == kFast ? launch_mode<kFast>(p, cfg, flags, s)
+                         : launch_mode<kExact>(p, cfg, flags, s);
 }
 
 cudaError_t read_clear_status_gemm(unsigned *out, cudaStream_t s) {

@@ -94,7 +94,9 @@ template <int MODE, class Cfg>
 __device__ __forceinline__ void mma_stage(Accum<Cfg> &acc, const float *As, const float *Bs,
                                           int arow0, int bcol0, int ty) {
     constexpr int TM = Cfg::TM, TN = Cfg::TN, BN = Cfg::BN;
-#pragma unroll
+    // Two of the eight 4-k chunks per loop body: enough independent work to
+    // hide shared-memory latency while keeping the loop in the instruction cache.
+#pragma unroll 2
     for (int kc = 0; kc < Cfg::BK / 4; ++kc) {
         float4 a[TM];
 #pragma unroll
@@ -151,6 +153,115 @@ struct TileRaster {
         tn = r / gsize;
     }
 };
+
+// ----------------------------------------------------------------- schedule
+// A CTA's work is a list of segments (tile, first k-stage, end k-stage, kind).
+//
+// Tiles [0, dp_tiles) are handed out round-robin, whole (data-parallel, in
+// the raster order that keeps concurrently running tiles close in L2).
+// The remaining tiles -- between one and two per CTA -- are balanced: their
+// units (tile, k-stage), tile-major, are cut into gridDim.x equal contiguous
+// ranges. A range can end inside a tile (its "early part": stages [0, e))
+// and start inside the tile the previous CTA ended in (its "late part":
+// stages [s, nk)). After its whole tiles a CTA runs its early part (from +0;
+// the raw accumulators are stored to the output and a flag is raised), then
+// the whole tiles of its range, then its late part, which waits for the
+// previous CTA's flag, loads the stored accumulators and continues from
+// them. This is the pages' k-block continuation: a later k-block starts from
+// the values the earlier blocks stored, and the stored value is the
+// accumulator itself, so every output still sees one sequential loop over k
+// from +0 and the bits equal the data-parallel schedule's. The previous CTA
+// stores its early part long before this CTA reaches its late part.
+enum SegKind : int { kSegFull = 0, kSegEarly = 1, kSegLate = 2 };
+
+struct Segment {
+    int tile, kb, ke, kind;
+};
+
+struct Schedule {
+    int tiles;         // output tiles (< 2^31)
+    int nk;            // k-stages per tile
+    int dp_tiles;      // tiles handed out whole; the rest are balanced
+    unsigned *flags;   // balanced part: flags[c] raised once CTA c's early part is stored
+
+    struct Local {
+        int count, dp_count, has_early, has_late;
+        int early_tile, late_tile, full0, early_ke, late_kb;
+    };
+
+    __device__ __forceinline__ Local local() const {
+        Local L{};
+        const int c = blockIdx.x, P = gridDim.x;
+        L.dp_count = (dp_tiles > c) ? (dp_tiles - 1 - c) / P + 1 : 0;
+        L.count = L.dp_count;
+        if (dp_tiles >= tiles) return L;
+        const int64_t U = static_cast<int64_t>(tiles - dp_tiles) * nk;
+        const int64_t lo = c * U / P, hi = (c + 1) * U / P;
+        L.has_late = (lo % nk) != 0;
+        L.late_tile = dp_tiles + static_cast<int>(lo / nk);
+        L.late_kb = static_cast<int>(lo % nk);
+        L.has_early = (hi % nk) != 0;
+        L.early_tile = dp_tiles + static_cast<int>(hi / nk);
+        L.early_ke = static_cast<int>(hi % nk);
+        L.full0 = dp_tiles + static_cast<int>((lo + nk - 1) / nk);
+        const int full1 = dp_tiles + static_cast<int>(hi / nk);
+        L.count += L.has_early + L.has_late + (full1 > L.full0 ? full1 - L.full0 : 0);
+        return L;
+    }
+
+    __device__ __forceinline__ Segment at(const Local &L, int i) const {
+        Segment s;
+        s.kb = 0;
+        s.ke = nk;
+        s.kind = kSegFull;
+        if (i < L.dp_count) {
+            s.tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            return s;
+        }
+        i -= L.dp_count;
+        if (L.has_early && i == 0) {
+            s.tile = L.early_tile;
+            s.ke = L.early_ke;
+            s.kind = kSegEarly;
+        } else if (L.has_late && i == L.count - L.dp_count - 1) {
+            s.tile = L.late_tile;
+            s.kb = L.late_kb;
+            s.kind = kSegLate;
+        } else {
+            s.tile = L.full0 + (i - L.has_early);
+        }
+        return s;
+    }
+};
+
+// Raise CTA blockIdx.x's flag after every consumer thread stored its part
+// (called by all consumer threads; named barrier 1 spans the consumers).
+__device__ __forceinline__ void signal_early_part(unsigned *flags, int consumers) {
+    asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicExch(&flags[blockIdx.x], 1u);
+    }
+}
+
+// Wait (bounded) for the previous CTA's early part; false on timeout.
+__device__ __forceinline__ bool wait_previous_part(unsigned *flags, int consumers, int *abort_flag) {
+    if (threadIdx.x == 0) {
+        const unsigned *f = flags + blockIdx.x - 1;
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+        if (v == 0) {
+            const unsigned long long t0 = global_ns();
+            do {
+                __nanosleep(200);
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+            } while (v == 0 && global_ns() - t0 <= kWaitLimitNs);
+        }
+        if (v == 0) *reinterpret_cast<volatile int *>(abort_flag) = 2;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
+    return *reinterpret_cast<volatile int *>(abort_flag) != 2;
+}
 
 template <class Cfg>
 __device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {

@@ -28,9 +28,9 @@
  * om_gemm_f32); it is never bit-exact.
  *
  * Conventions for every entry point:
- *   - Pointers named A, B, C, x, w, w_packed, y are DEVICE pointers to memory
- *     owned by the caller. The library allocates no device memory and keeps
- *     no per-call state; it only caches device properties.
+ *   - Pointers named A, B, C, x, w, w_packed, y, workspace are DEVICE
+ *     pointers to memory owned by the caller. The library allocates no device
+ *     memory and keeps no per-call state; it only caches device properties.
  *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream). Calls are asynchronous on that stream and never synchronise;
  *     a kernel fault surfaces on the stream as CUDA reports it.
@@ -121,6 +121,39 @@ OM_API int om_gemm_f32(int64_t m, int64_t n, int64_t k,
                        int mode, void *stream);
 
 /*
+ * Bytes of device scratch the *_ws entry points need (a constant: one 32-bit
+ * flag per CTA of the balanced schedule, for grids of up to 1024 CTAs).
+ */
+OM_API size_t om_workspace_bytes(void);
+
+/*
+ * om_gemm_f32 with caller scratch for a balanced schedule. Output tiles are
+ * handed out whole for all but the last one or two rounds of the SMs; the
+ * k-loops of the remaining tiles are cut into equal contiguous ranges, one
+ * per SM. A range that ends inside a tile computes that tile's first
+ * k-stages and stores the raw accumulators to C; the next range finishes the
+ * tile from those stored accumulators ("Matrix product and convolution
+ * kernels" page, item 3 "Microkernel": a later k-block starts from the C
+ * values the earlier blocks stored). Every output is still one sequential
+ * loop over k from +0, so the bits are identical to om_gemm_f32; only the
+ * load balance across SMs changes (no idle SMs in a last, partial round).
+ *   workspace: device memory, 16-byte aligned, at least om_workspace_bytes(),
+ *   not overlapping A, B or C. The call clears what it uses on stream before
+ *   the kernel runs. Calls that may run at the same time on the GPU need
+ *   distinct workspaces.
+ * Problems whose tiles fill whole rounds of the SMs, or that have fewer tiles
+ * than SMs, run the plain schedule. Errors as om_gemm_f32, plus
+ * OM_ERR_NULL_PTR for a NULL workspace, OM_ERR_INVALID_ARG for a short one
+ * and OM_ERR_ALIGNMENT for a misaligned one. OM_MODE_TF32X3 ignores the
+ * workspace.
+ */
+OM_API int om_gemm_f32_ws(int64_t m, int64_t n, int64_t k,
+                          const float *A, int64_t lda,
+                          const float *B, int64_t ldb,
+                          float *C, int64_t ldc,
+                          int mode, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * 2-D convolution, NCHW ("Exact mode", section "Convolution"; "Convolution
  * (fast mode)", section "What each output is"), computed as an implicit
  * matrix product: per image and group, A = the group's weights
@@ -144,6 +177,18 @@ OM_API int om_conv2d_f32(int64_t N, int64_t Cin, int64_t H, int64_t W,
                          int64_t stride, int64_t pad, int64_t dil,
                          const float *x, const float *w, float *y,
                          int mode, void *stream);
+
+/*
+ * om_conv2d_f32 with caller scratch for the balanced schedule (as
+ * om_gemm_f32_ws: the taps of the last output tiles are split evenly over the
+ * SMs with k-block continuation through y). Bit-identical to om_conv2d_f32.
+ * Workspace rules and extra errors as om_gemm_f32_ws.
+ */
+OM_API int om_conv2d_f32_ws(int64_t N, int64_t Cin, int64_t H, int64_t W,
+                            int64_t Cout, int64_t G, int64_t KH, int64_t KW,
+                            int64_t stride, int64_t pad, int64_t dil,
+                            const float *x, const float *w, float *y,
+                            int mode, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Re-lays out convolution weights once for om_conv2d_f32_packed
@@ -172,6 +217,14 @@ OM_API int om_conv2d_f32_packed(int64_t N, int64_t Cin, int64_t H, int64_t W,
                                 int64_t stride, int64_t pad, int64_t dil,
                                 const float *x, const float *w_packed, float *y,
                                 int mode, void *stream);
+
+/* om_conv2d_f32_packed with caller scratch for the balanced schedule. */
+OM_API int om_conv2d_f32_packed_ws(int64_t N, int64_t Cin, int64_t H, int64_t W,
+                                   int64_t Cout, int64_t G, int64_t KH, int64_t KW,
+                                   int64_t stride, int64_t pad, int64_t dil,
+                                   const float *x, const float *w_packed, float *y,
+                                   int mode, void *workspace, size_t workspace_bytes,
+                                   void *stream);
 
 /*
  * Synchronises stream, then reads and clears the library's device status

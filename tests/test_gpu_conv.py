@@ -21,7 +21,7 @@ def built():
     oracle.build()
 
 
-def run_conv(c: synth.ConvCase, name, cfg=None, packed=False):
+def run_conv(c: synth.ConvCase, name, cfg=None, packed=False, workspace=None):
     import torch
     x, w = to_dev(c.x), to_dev(c.w)
     OH = oracle.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.pad, c.dil)
@@ -32,13 +32,19 @@ def run_conv(c: synth.ConvCase, name, cfg=None, packed=False):
     with forced_config("OM_FORCE_CONV_CFG", cfg):
         if packed:
             wp = om.pack_conv_weights(w, c.G)
-            st = om.lib().om_conv2d_f32_packed(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW,
-                                               c.stride, c.pad, c.dil, x.data_ptr(), wp.data_ptr(),
-                                               y.data_ptr(), om.MODES[name], None)
+            args = (c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad, c.dil,
+                    x.data_ptr(), wp.data_ptr(), y.data_ptr(), om.MODES[name])
+            if workspace is None:
+                st = om.lib().om_conv2d_f32_packed(*args, None)
+            else:
+                st = om.lib().om_conv2d_f32_packed_ws(*args, workspace.data_ptr(), 4096, None)
         else:
-            st = om.lib().om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride,
-                                        c.pad, c.dil, x.data_ptr(), w.data_ptr(), y.data_ptr(),
-                                        om.MODES[name], None)
+            args = (c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad, c.dil,
+                    x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[name])
+            if workspace is None:
+                st = om.lib().om_conv2d_f32(*args, None)
+            else:
+                st = om.lib().om_conv2d_f32_ws(*args, workspace.data_ptr(), 4096, None)
     assert st == 0, om.STATUS_NAMES.get(st, st)
     torch.cuda.synchronize()
     assert om.device_status() == 0
@@ -127,3 +133,29 @@ def test_empty_input_channels_give_plus_zero():
     assert st == 0
     torch.cuda.synchronize()
     assert (y.cpu().numpy().view(np.uint32) == 0).all()
+
+
+# ---- balanced schedule (om_conv2d_f32_ws): k-block continuation across CTAs
+@pytest.mark.parametrize("which", ["conv3x3", "conv1x1", "grouped"])
+@pytest.mark.parametrize("mode,name", MODES)
+def test_workspace_schedule_is_bit_identical(which, mode, name):
+    c = {"conv3x3": synth.workload_conv3x3, "conv1x1": synth.workload_conv1x1,
+         "grouped": synth.workload_conv_grouped}[which]()
+    ws = om.new_workspace()
+    plain = run_conv(c, name, 0)  # the direct kernel
+    for cfg in (None, 1):
+        assert_bits_equal(run_conv(c, name, cfg, workspace=ws), plain, f"{which} ws cfg={cfg}")
+    got = run_conv(c, name, None, packed=True, workspace=ws)
+    assert_bits_equal(got, plain, f"{which} packed ws")
+    assert_bits_equal(got[:1], want_conv(c, mode, (0, 1)), f"{which} image 0 vs oracle")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_workspace_odd_geometry(mode, name):
+    # ragged columns, K = 81 (not a multiple of 32 or 4: 4-byte weight path), 3 groups
+    c = synth.make_conv("t", 20, 27, 33, 31, 96, 3, 3, 3, 1, 1, 1, seed=90,
+                        dist_x=("uniform", -1, 1), dist_w=("normal", 0, 0.3))
+    ws = om.new_workspace()
+    want = want_conv(c, mode)
+    for cfg in (None, 1):
+        assert_bits_equal(run_conv(c, name, cfg, workspace=ws), want, f"odd ws cfg={cfg}")

@@ -172,3 +172,68 @@ def test_fast_mode_error_bound_4096_rows():
     got = C.cpu().numpy()[:2].astype(np.float64)
     ref, mag = oracle.gemm_f64(case.A[:2], case.B, oracle.default_threads())
     assert (np.abs(got - ref) <= case.k * 2.0 ** -24 * mag + 1e-30).all()
+
+
+# ---- balanced schedule (om_gemm_f32_ws): k-block continuation across CTAs
+WS_SHAPES = [
+    # (m, n, k): more tiles than SMs, not whole rounds, so the last rounds are split
+    (2048, 2560, 1000), (4096, 4096, 4096), (1300, 5000, 333), (640, 7700, 64),
+    (512, 11008, 4096),
+]
+
+
+@pytest.mark.parametrize("shape", WS_SHAPES)
+@pytest.mark.parametrize("mode,name", MODES)
+def test_workspace_schedule_is_bit_identical(shape, mode, name):
+    import torch
+    m, n, k = shape
+    case = synth.make_gemm("ws", m, n, k, seed=m + n + k, dist_a=("normal", 0, 1),
+                           dist_b=("normal", 0, 1))
+    A, B = to_dev(case.A), to_dev(case.B)
+    ws = om.new_workspace()
+    plain = om.gemm(A, B, mode=name).cpu().numpy()
+    for cfg in (None, 2, 4):
+        with forced_config("OM_FORCE_GEMM_CFG", cfg):
+            C = torch.full((m, n), float("nan"), device="cuda")
+            om.gemm(A, B, out=C, mode=name, workspace=ws)
+            assert_bits_equal(C.cpu().numpy(), plain, f"ws vs plain {shape} cfg={cfg}")
+    torch.cuda.synchronize()
+    assert om.device_status() == 0
+    for r0 in (0, m // 2, m - 1):
+        assert_bits_equal(plain[r0:r0 + 1], oracle_case(case, mode, (r0, r0 + 1)), f"rows {r0}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_workspace_with_specials_and_padding(mode, name):
+    # strided operands (4-byte producer) and IEEE specials through the balanced schedule
+    import torch
+    case = synth.make_gemm("wsp", 1500, 3000, 200, lda=203, ldb=3001, ldc=3003, seed=77,
+                           special_cells=8)
+    A, B = to_dev(case.A), to_dev(case.B)
+    buf, C = guarded_output(case.C_init)
+    ws = om.new_workspace()
+    st = om.gemm_raw(case.m, case.n, case.k, A.data_ptr(), case.lda, B.data_ptr(), case.ldb,
+                     C.data_ptr(), case.ldc, name, workspace=ws)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert guards_intact(buf)
+    got = C.cpu().numpy().reshape(case.C_init.shape)
+    assert (bits(got)[:, case.n:] == synth.C_SENTINEL_BITS).all()
+    plain, ok = run_case(case, name)
+    assert_bits_equal(got, plain, "ws vs plain strided")
+    for r in sorted({case.special["A_cells"][0] // case.k, 0, case.m - 1}):
+        assert_bits_equal(got[r:r + 1], oracle_case(case, mode, (r, r + 1)), f"row {r}")
+
+
+def test_workspace_validation():
+    import torch
+    ws = om.new_workspace()
+    A = torch.zeros((64, 64), device="cuda")
+    C = torch.zeros((64, 64), device="cuda")
+    L = om.lib()
+    args = (64, 64, 64, A.data_ptr(), 64, A.data_ptr(), 64, C.data_ptr(), 64, 0)
+    assert L.om_gemm_f32_ws(*args, None, 4096, None) == 2
+    assert L.om_gemm_f32_ws(*args, ws.data_ptr(), 16, None) == 1
+    assert L.om_gemm_f32_ws(*args, ws.data_ptr() + 4, 8192, None) == 7
+    assert L.om_gemm_f32_ws(*args, C.data_ptr(), 16384, None) == 3  # workspace inside C
+    assert om.workspace_bytes() == 4096
