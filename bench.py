@@ -1,7 +1,8 @@
 """Benchmark: GFLOP/s and fraction of the FP32 CUDA-core roofline.
 
 Headline (``value``): the exact-mode fp32 product C = A*B at m = n = k = 4096
-(A, B ~ N(0, 1), row-major, contiguous), one om_gemm_f32 call per step,
+(A, B ~ N(0, 1), row-major, contiguous), one om_gemm_f32_ws call per step
+(the balanced schedule; om_gemm_f32 without scratch is reported beside it),
 inputs resident in HBM, L2 flushed (a 512 MiB write) before every timed
 call. Also reported per step set: fast mode on the same product, the
 ResNet-50 stage-1 3x3 and 1x1 convolutions (exact and fast), the prefill
@@ -224,8 +225,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     B = torch.from_numpy(case.B).to(dev)
     C = torch.empty((m, n), dtype=torch.float32, device=dev)
 
+    ws = om.new_workspace(dev)
+
     def step_exact():
-        st = om.gemm_raw(m, n, k, A.data_ptr(), k, B.data_ptr(), n, C.data_ptr(), n, "exact", stream)
+        st = om.gemm_raw(m, n, k, A.data_ptr(), k, B.data_ptr(), n, C.data_ptr(), n, "exact", stream,
+                         workspace=ws)
         if st != 0:
             raise RuntimeError(f"om_gemm_f32 failed: {om.STATUS_NAMES.get(st, st)}")
 
@@ -277,7 +281,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         dA.copy_(hA, non_blocking=True)
         dB.copy_(hB, non_blocking=True)
         st = om.gemm_raw(m, n, k, dA.data_ptr(), k, dB.data_ptr(), n, C.data_ptr(), n, "exact",
-                         stream)
+                         stream, workspace=ws)
         if st != 0:
             raise RuntimeError("om_gemm_f32 failed")
         hC.copy_(C, non_blocking=True)
@@ -358,9 +362,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
 
     if not args.headline_only:
-        gemm_line("gemm_4096^3_fast", "fast", case)
-        gemm_line("gemm_4096^3_exact_ws", "exact", case, use_ws=True)
         gemm_line("gemm_4096^3_fast_ws", "fast", case, use_ws=True)
+        gemm_line("gemm_4096^3_exact_no_workspace", "exact", case)
+        gemm_line("gemm_4096^3_fast_no_workspace", "fast", case)
         tf32x3_line("gemm_4096^3_tf32x3", case)
         gemm_line("gemm_prefill_512x11008x4096_exact_ws", "exact",
                   synth.workload_gemm_prefill(False), use_ws=True)
@@ -393,6 +397,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "dtype": "f32",
         "data": "synthetic (seeded SplitMix64, N(0,1) operands)",
         "config": {"workload": "gemm_4096^3", "m": m, "n": n, "k": k, "mode": "exact",
+                   "entry_point": "om_gemm_f32_ws",
                    "layout": "row-major contiguous", "l2": "flushed before every timed call",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "alu", "achieved": round(achieved_tflops, 3),
@@ -490,9 +495,11 @@ def run_profile(args):
         B = torch.from_numpy(case.B).to(dev)
         C = torch.from_numpy(case.C_init).to(dev)
 
+        ws = om.new_workspace(dev)
+
         def f():
             st = om.gemm_raw(case.m, case.n, case.k, A.data_ptr(), case.lda, B.data_ptr(),
-                             case.ldb, C.data_ptr(), case.ldc, mode, stream)
+                             case.ldb, C.data_ptr(), case.ldc, mode, stream, workspace=ws)
             assert st == 0, st
     else:
         c = convs[name]()
@@ -502,10 +509,13 @@ def run_profile(args):
         OW = om.conv_out_dim(c.W, c.KW, c.stride, c.pad, c.dil)
         y = torch.empty((c.N, c.Cout, OH, OW), dtype=torch.float32, device=dev)
 
+        ws = om.new_workspace(dev)
+
         def f():
-            st = L.om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad,
-                                 c.dil, x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[mode],
-                                 stream.cuda_stream)
+            st = L.om_conv2d_f32_ws(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride,
+                                    c.pad, c.dil, x.data_ptr(), w.data_ptr(), y.data_ptr(),
+                                    om.MODES[mode], ws.data_ptr(), om.workspace_bytes(),
+                                    stream.cuda_stream)
             assert st == 0, st
     for _ in range(args.warmup + args.steps):
         f()
