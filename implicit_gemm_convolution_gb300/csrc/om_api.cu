@@ -233,6 +233,18 @@ int conv_impl(const ConvArgs &a, const float *x, const float *w, bool packed, fl
 
 }  // namespace
 
+namespace om {
+
+// The argument checks and dispatch of om_gemm_f32_ws, for other entry points
+// of the library that supply the scratch themselves.
+int gemm_with_scratch(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda,
+                      const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+                      void *scratch, size_t scratch_bytes, void *stream) {
+    return gemm_impl(m, n, k, A, lda, B, ldb, C, ldc, mode, scratch, scratch_bytes, stream);
+}
+
+}  // namespace om
+
 extern "C" {
 
 int om_version(void) { return OM_VERSION; }

@@ -69,6 +69,12 @@ cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, unsign
 cudaError_t launch_gemm_tf32x3(const GemmProblem &p, cudaStream_t s);
 cudaError_t read_clear_status_tc(unsigned *out, cudaStream_t s);
 
+// The checks and dispatch of om_gemm_f32_ws with scratch supplied by the
+// library itself (see om_gemm_f32_no_alloc).
+int gemm_with_scratch(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda,
+                      const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+                      void *scratch, size_t scratch_bytes, void *stream);
+
 // Read and clear the device status word of the tiled translation units
 // (synchronises s).
 cudaError_t read_clear_status_gemm(unsigned *out, cudaStream_t s);

@@ -154,6 +154,34 @@ OM_API int om_gemm_f32_ws(int64_t m, int64_t n, int64_t k,
                           int mode, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * om_gemm_f32_ws for callers that cannot allocate device memory. The paper has
+ * no counterpart: it describes CPU kernels, with no device memory to manage.
+ * Some callers of a GPU library may not call cudaMalloc at all: plugins and
+ * kernels run by a host framework that hands out only buffers it planned
+ * itself, or latency-critical paths where an allocation (and the
+ * synchronisation it can bring) is not allowed. They pass only A, B and C.
+ * Same arguments, results (bit for bit) and errors as om_gemm_f32 /
+ * om_gemm_f32_ws.
+ * Scratch: the balanced schedule's flags live in a 4 KiB static device array
+ * (1024 words, one per SM used) that every GPU loading the library holds
+ * until the process exits. OM_ERR_TOO_LARGE if the device has more than 1024
+ * SMs.
+ * The first call on a device looks up that array's device address with the
+ * device current (cudaGetSymbolAddress); make that first call before any
+ * stream capture. No call allocates or frees device memory.
+ * All calls share the one array and it keeps the previous call's contents;
+ * each call clears the words it needs on its stream before its kernel runs.
+ * Calls that may overlap on the GPU (other streams, other threads) race on
+ * the array: run them on one stream, or use om_gemm_f32_ws with a workspace
+ * per stream.
+ */
+OM_API int om_gemm_f32_no_alloc(int64_t m, int64_t n, int64_t k,
+                                const float *A, int64_t lda,
+                                const float *B, int64_t ldb,
+                                float *C, int64_t ldc,
+                                int mode, void *stream);
+
+/*
  * 2-D convolution, NCHW ("Exact mode", section "Convolution"; "Convolution
  * (fast mode)", section "What each output is"), computed as an implicit
  * matrix product: per image and group, A = the group's weights
