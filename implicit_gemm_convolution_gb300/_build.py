@@ -45,16 +45,28 @@ def _inputs() -> list[str]:
     return files
 
 
+def _stamp() -> str:
+    return " ".join(_extra_flags())
+
+
 def is_stale() -> bool:
     if not os.path.exists(LIB_PATH):
+        return True
+    stamp = LIB_PATH + ".flags"
+    if (open(stamp).read() if os.path.exists(stamp) else "") != _stamp():
         return True
     t = os.path.getmtime(LIB_PATH)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
+def _extra_flags() -> list[str]:
+    """Extra nvcc flags for tuning builds (OM_EXTRA_NVCC_FLAGS, space separated)."""
+    return os.environ.get("OM_EXTRA_NVCC_FLAGS", "").split()
+
+
 def _compile(src: str) -> str:
     obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-    cmd = [nvcc(), *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    cmd = [nvcc(), *NVCC_FLAGS, *_extra_flags(), "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -76,4 +88,6 @@ def build(force: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(LIB_PATH + ".flags", "w") as f:
+        f.write(_stamp())
     return LIB_PATH

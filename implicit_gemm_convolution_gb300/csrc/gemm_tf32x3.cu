@@ -149,8 +149,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                        int tiles_n, int vec_store) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
-    Smem sm{reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                        ~static_cast<uintptr_t>(1023))};
+    Smem sm{smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u)};
     Bars *bars = reinterpret_cast<Bars *>(sm.base + S_F32 * F32_STAGE + S_OPS * OPS_STAGE);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int total = tiles_m * tiles_n;

@@ -18,7 +18,19 @@
 
 #include "om_device.cuh"
 
+// 4-k chunks of a 32-k stage per unrolled loop body, per mode (tuning knobs).
+#ifndef OM_KC_UNROLL_EXACT
+#define OM_KC_UNROLL_EXACT 2
+#endif
+#ifndef OM_KC_UNROLL_FAST
+#define OM_KC_UNROLL_FAST 8
+#endif
+
+
 namespace om {
+
+constexpr int kKcUnrollExact = OM_KC_UNROLL_EXACT;
+constexpr int kKcUnrollFast = OM_KC_UNROLL_FAST;
 
 template <int BM_, int BN_, int TM_, int TN_, int WARPS_M_, int WARPS_N_, int STAGES_, bool X2_>
 struct TileCfg {
@@ -94,9 +106,9 @@ template <int MODE, class Cfg>
 __device__ __forceinline__ void mma_stage(Accum<Cfg> &acc, const float *As, const float *Bs,
                                           int arow0, int bcol0, int ty) {
     constexpr int TM = Cfg::TM, TN = Cfg::TN, BN = Cfg::BN;
-    // Two of the eight 4-k chunks per loop body: enough independent work to
+    // A few of the eight 4-k chunks per loop body: enough independent work to
     // hide shared-memory latency while keeping the loop in the instruction cache.
-#pragma unroll 2
+#pragma unroll(MODE == kFast ? kKcUnrollFast : kKcUnrollExact)
     for (int kc = 0; kc < Cfg::BK / 4; ++kc) {
         float4 a[TM];
 #pragma unroll
@@ -263,10 +275,15 @@ __device__ __forceinline__ bool wait_previous_part(unsigned *flags, int consumer
     return *reinterpret_cast<volatile int *>(abort_flag) != 2;
 }
 
+// The dynamic shared-memory base advanced to a 1024-byte boundary (what the
+// 128B swizzle pattern repeats on). The offset is added to the shared pointer
+// itself, so the compiler keeps knowing the address is shared memory and
+// emits shared loads (an integer round trip would turn them into generic
+// loads through the L1 path).
 template <class Cfg>
 __device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) &
-                                       ~static_cast<uintptr_t>(1023));
+    const uint32_t base = smem_u32(raw);
+    return raw + ((1024u - (base & 1023u)) & 1023u);
 }
 
 }  // namespace om
