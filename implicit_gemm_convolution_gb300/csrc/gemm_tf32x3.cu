@@ -103,6 +103,25 @@ __device__ __forceinline__ void split(float a, float &hi, float &lo) {
     lo = isfinite(fh) ? __uint_as_float(l) : 0.0f;
 }
 
+// Explicit shared-memory accesses on 32-bit shared addresses.
+__device__ __forceinline__ float4 lds128(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
 struct Smem {
     uint8_t *base;
     __device__ uint8_t *a32(int s) const { return base + s * F32_STAGE; }
@@ -264,22 +283,21 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
             for (int kt = 0; kt < nk; ++kt) {
                 if (!wait(bars, &bars->full_f[sf], phf)) break;
                 if (!wait(bars, &bars->empty_o[so], pho ^ 1)) break;
-                const uint8_t *a32 = sm.a32(sf);
-                const float *b32 = reinterpret_cast<const float *>(sm.b32(sf));
-                uint8_t *ahi = sm.ops(so, 0), *alo = sm.ops(so, 1);
-                uint8_t *bhi = sm.ops(so, 2), *blo = sm.ops(so, 3);
+                const uint32_t a32 = smem_u32(sm.a32(sf)), b32 = smem_u32(sm.b32(sf));
+                const uint32_t ahi = smem_u32(sm.ops(so, 0)), alo = smem_u32(sm.ops(so, 1));
+                const uint32_t bhi = smem_u32(sm.ops(so, 2)), blo = smem_u32(sm.ops(so, 3));
                 // A: same 128B-swizzled K-major layout, 16-byte chunks
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int off = (ct + kConvThreads * i) * 16;
-                    const float4 v = *reinterpret_cast<const float4 *>(a32 + off);
+                    const uint32_t off = static_cast<uint32_t>((ct + kConvThreads * i) * 16);
+                    const float4 v = lds128(a32 + off);
                     float4 h, l;
                     split(v.x, h.x, l.x);
                     split(v.y, h.y, l.y);
                     split(v.z, h.z, l.z);
                     split(v.w, h.w, l.w);
-                    *reinterpret_cast<float4 *>(ahi + off) = h;
-                    *reinterpret_cast<float4 *>(alo + off) = l;
+                    sts128(ahi + off, h);
+                    sts128(alo + off, l);
                 }
                 // B: [32 k][128 n] row-major -> [128 n][32 k] 128B-swizzled
                 const int n = ct % BN;
@@ -288,13 +306,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                     const int kc = kc0 + i;
                     float4 h, l;
-                    split(b32[(4 * kc + 0) * BN + n], h.x, l.x);
-                    split(b32[(4 * kc + 1) * BN + n], h.y, l.y);
-                    split(b32[(4 * kc + 2) * BN + n], h.z, l.z);
-                    split(b32[(4 * kc + 3) * BN + n], h.w, l.w);
-                    const int off = n * 128 + ((kc ^ (n & 7)) << 4);
-                    *reinterpret_cast<float4 *>(bhi + off) = h;
-                    *reinterpret_cast<float4 *>(blo + off) = l;
+                    split(lds32(b32 + ((4 * kc + 0) * BN + n) * 4), h.x, l.x);
+                    split(lds32(b32 + ((4 * kc + 1) * BN + n) * 4), h.y, l.y);
+                    split(lds32(b32 + ((4 * kc + 2) * BN + n) * 4), h.z, l.z);
+                    split(lds32(b32 + ((4 * kc + 3) * BN + n) * 4), h.w, l.w);
+                    const uint32_t off = static_cast<uint32_t>(n * 128 + ((kc ^ (n & 7)) << 4));
+                    sts128(bhi + off, h);
+                    sts128(blo + off, l);
                 }
                 fence_proxy_async_smem();  // generic writes -> tensor-core reads
                 __syncwarp();

@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_conv2d_f32.argtypes = [i64] * 16 + [fp, fp, fp, ci, ci]
             L.oracle_conv2d_f64.restype = None
             L.oracle_conv2d_f64.argtypes = [i64] * 16 + [fp, fp, dp, dp, ci]
+            L.oracle_epilogue_f32.restype = None
+            L.oracle_epilogue_f32.argtypes = [i64, i64, i64, fp, fp, fp, ci]
             rc = L.oracle_selfcheck()
             if rc != 0:
                 raise RuntimeError(f"oracle self-check failed with code {rc}: host float "
@@ -166,3 +168,22 @@ def conv2d_f64(x, w, stride=1, pad=0, dil=1, groups=1, threads=1):
     if ref.size and x.size and w.size:
         lib().oracle_conv2d_f64(*args, _ptr(x), _ptr(w), _ptr(ref), _ptr(mag), threads)
     return ref, mag
+
+
+RELU = 1
+
+
+def epilogue(y: np.ndarray, bias=None, res=None, activation: int = 0, channel_axis: int = 1):
+    """Bias (per channel_axis index), then residual, then activation, on a copy
+    of y (a product's output with channel_axis=1 for per-column bias of a 2-D
+    matrix, or a convolution's NCHW output with channel_axis=1)."""
+    y = np.ascontiguousarray(y, dtype=np.float32).copy()
+    if y.size == 0:
+        return y
+    channels = y.shape[channel_axis]
+    plane = int(np.prod(y.shape[channel_axis + 1:])) if y.ndim > channel_axis + 1 else 1
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    r = None if res is None else np.ascontiguousarray(res, dtype=np.float32)
+    lib().oracle_epilogue_f32(y.size, plane, channels, _ptr(y), None if b is None else _ptr(b),
+                              None if r is None else _ptr(r), int(activation))
+    return y

@@ -224,3 +224,28 @@ void oracle_conv2d_f64(int64_t N, int64_t Cin, int64_t H, int64_t W,
         }
     }
 }
+
+/*
+ * Output epilogue ("Convolution (fast mode)", section "Tiles and chunks": the
+ * epilogue, bias then activation, applied to each finished tile, rows counted
+ * from the group's first output channel; section "Single-column products":
+ * the bias, activation and residual epilogue). The pages do not fix where the
+ * residual goes relative to the activation; the reading taken here is bias,
+ * then residual, then activation, each one binary32 operation:
+ *   v = y; v = v + bias[ch]; v = v + res; v = relu(v); store canonical(v)
+ * with relu(v) = v for v > 0 or NaN, +0 otherwise (so relu(-0) = +0).
+ * y holds `count` outputs; output o belongs to channel (o / plane) % channels
+ * (plane = OH*OW, channels = Cout for a convolution; plane = 1, channels = n
+ * for a row-major m x n product, where the bias is per column). bias and res
+ * may be NULL; res has y's layout. activation: 0 none, 1 ReLU.
+ */
+void oracle_epilogue_f32(int64_t count, int64_t plane, int64_t channels, float *y,
+                         const float *bias, const float *res, int activation) {
+    for (int64_t o = 0; o < count; ++o) {
+        float v = y[o];
+        if (bias) v = v + bias[(o / plane) % channels];
+        if (res) v = v + res[o];
+        if (activation == 1 && !(v > 0.0f) && !isnan(v)) v = +0.0f;
+        y[o] = canonical(v);
+    }
+}

@@ -44,6 +44,13 @@ MUTANTS = {
     "conv_pad_sign": ("                                const int64_t iy = oy * sH - pT + ky * dH;\n                                const int64_t ix = ox * sW - pL + kx * dW;\n                                float v",
                       "                                const int64_t iy = oy * sH + pT + ky * dH;\n                                const int64_t ix = ox * sW - pL + kx * dW;\n                                float v"),
     "out_dim_off_by_one": ("    return num / stride + 1;", "    return (num + 1) / stride + 1;"),
+    "epilogue_relu_before_residual": (
+        "        if (res) v = v + res[o];\n        if (activation == 1 && !(v > 0.0f) && !isnan(v)) v = +0.0f;",
+        "        if (activation == 1 && !(v > 0.0f) && !isnan(v)) v = +0.0f;\n        if (res) v = v + res[o];"),
+    "epilogue_bias_plus_residual_first": (
+        "        if (bias) v = v + bias[(o / plane) % channels];\n        if (res) v = v + res[o];",
+        "        if (bias && res) v = v + (bias[(o / plane) % channels] + res[o]);\n        else if (bias) v = v + bias[(o / plane) % channels];\n        else if (res) v = v + res[o];"),
+    "epilogue_relu_drops_nan": ("!(v > 0.0f) && !isnan(v)", "!(v > 0.0f)"),
 }
 
 
@@ -62,6 +69,8 @@ def _build(tmp_path, name, old, new):
     L.oracle_conv2d_f32.argtypes = [i64] * 16 + [vp, vp, vp, ci, ci]
     L.oracle_conv_out_dim.argtypes = [i64] * 6
     L.oracle_conv_out_dim.restype = i64
+    L.oracle_epilogue_f32.argtypes = [i64, i64, i64, vp, vp, vp, ci]
+    L.oracle_epilogue_f32.restype = None
     return L
 
 
@@ -109,6 +118,22 @@ def _pins_pass(L) -> bool:
                             s["stride"], s["stride"], s["pad"], s["pad"], s["pad"], s["pad"],
                             s["dil"], s["dil"], x.ctypes.data, w.ctypes.data, y.ctypes.data, 0, 1)
         if y[:len(pin["exact_bits"])].view(np.uint32).tolist() != pin["exact_bits"]:
+            return False
+    e = json.load(open(os.path.join(HERE, "golden", "epilogue_pins.json")))
+    for pin in e["pins"]:
+        y = np.array(pin["y"], np.float32)
+        shape = pin.get("shape", [1, len(pin["y"])])
+        channels = shape[1]
+        plane = int(np.prod(shape[2:])) if len(shape) > 2 else 1
+        bias = pin["bias"]
+        if bias is not None and "shape" not in pin:
+            bias = bias * channels
+        b = None if bias is None else np.array(bias, np.float32)
+        r = None if pin["res"] is None else np.array(pin["res"], np.float32)
+        L.oracle_epilogue_f32(y.size, plane, channels, y.ctypes.data,
+                              None if b is None else b.ctypes.data,
+                              None if r is None else r.ctypes.data, pin["act"])
+        if y.view(np.uint32).tolist() != pin["out_bits"]:
             return False
     for cs in c["out_dims"]["cases"]:
         if L.oracle_conv_out_dim(cs["size"], cs["k"], cs["stride"], cs["pad"], cs["pad"], cs["dil"]) != cs["out"]:

@@ -337,3 +337,47 @@ def test_conv_thread_count_does_not_change_bits():
     case = synth.make_conv("t", 3, 8, 10, 10, 8, 2, 3, 3, 1, 1, 1, seed=42)
     ys = [bits(oracle.conv2d(case.x, case.w, 1, 1, 1, 2, 0, t)).copy() for t in (1, 4)]
     assert (ys[0] == ys[1]).all()
+
+
+# --- output epilogue (bias, residual, ReLU) ---------------------------------
+def test_golden_epilogue_pins():
+    d = json.load(open(os.path.join(GOLDEN, "epilogue_pins.json")))
+    for pin in d["pins"]:
+        y = np.array(pin["y"], np.float32)
+        if "shape" in pin:
+            y = y.reshape(pin["shape"])
+        else:
+            y = y.reshape(1, -1)
+        bias = None if pin["bias"] is None else np.array(pin["bias"], np.float32)
+        res = None if pin["res"] is None else np.array(pin["res"], np.float32).reshape(y.shape)
+        if bias is not None and "shape" not in pin:
+            bias = np.full(y.shape[1], bias[0], np.float32)
+        out = oracle.epilogue(y, bias, res, pin["act"])
+        assert bits(out).reshape(-1).tolist() == pin["out_bits"], pin["name"]
+
+
+def test_epilogue_matches_rational_model():
+    rng = np.random.default_rng(33)
+    y = (rng.standard_normal((6, 7)) * 10).astype(np.float32)
+    bias = (rng.standard_normal(7) * 10).astype(np.float32)
+    res = (rng.standard_normal((6, 7)) * 10).astype(np.float32)
+    out = oracle.epilogue(y, bias, res, oracle.RELU)
+    for i in range(6):
+        for j in range(7):
+            v = ieee_ref.add(ieee_ref.add(float(y[i, j]), float(bias[j])), float(res[i, j]))
+            v = v if (v > 0 or math.isnan(v)) else 0.0
+            assert bits(out)[i, j] == ieee_ref.canonical_bits(v)
+
+
+def test_epilogue_on_conv_equals_torch_with_integers():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(34)
+    x = rng.integers(-3, 4, (2, 4, 6, 6)).astype(np.float32)
+    w = rng.integers(-3, 4, (6, 4, 3, 3)).astype(np.float32)
+    b = rng.integers(-20, 21, 6).astype(np.float32)
+    r = rng.integers(-20, 21, (2, 6, 6, 6)).astype(np.float32)
+    y = oracle.epilogue(oracle.conv2d(x, w, 1, 1, 1, 1), b, r, oracle.RELU)
+    t = torch.nn.functional.conv2d(torch.from_numpy(x).double(), torch.from_numpy(w).double(),
+                                   torch.from_numpy(b).double(), padding=1)
+    t = torch.relu(t + torch.from_numpy(r).double())
+    assert np.array_equal(y.astype(np.float64), t.numpy())
