@@ -32,6 +32,7 @@ STATUS_NAMES = {
     8: "OM_ERR_TOO_LARGE",
 }
 MODES = {"exact": 0, "fast": 1, "tf32x3": 2}
+ACTIVATIONS = {None: 0, "none": 0, "relu": 1}
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +85,12 @@ def lib() -> ctypes.CDLL:
             L.om_device_status.restype = ci
             L.om_device_status.argtypes = [vp]
             L.om_workspace_bytes.restype = ctypes.c_size_t
+            L.om_gemm_f32_ex.restype = ci
+            L.om_gemm_f32_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp, i64, ci,
+                                         ci, vp, ctypes.c_size_t, vp]
+            L.om_conv2d_f32_ex.restype = ci
+            L.om_conv2d_f32_ex.argtypes = [i64] * 11 + [vp, vp, ci, vp, vp, ci, vp, ci, vp,
+                                                        ctypes.c_size_t, vp]
             L.om_gemm_f32_ws.restype = ci
             L.om_gemm_f32_ws.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, vp,
                                          ctypes.c_size_t, vp]
@@ -264,3 +271,52 @@ def conv2d_packed(x, w_packed, w_shape, stride: int = 1, padding: int = 0, dilat
 def device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status word."""
     return int(lib().om_device_status(_stream_handle(stream)))
+
+
+def _ptr_or_none(t):
+    return None if t is None else t.data_ptr()
+
+
+def gemm_ex(A, B, bias=None, residual=None, activation=None, out=None, mode="exact",
+            stream=None, workspace=None):
+    """act(A @ B + bias + residual): bias per column (n,), residual (m, n)."""
+    import torch
+    _require(A, "A", 2)
+    _require(B, "B", 2)
+    m, k = A.shape
+    n = B.shape[1]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float32, device=A.device)
+    if bias is not None:
+        _require(bias, "bias", 1)
+    if residual is not None:
+        _require(residual, "residual", 2)
+    lda = A.stride(0) if m > 1 else max(k, 1)
+    ldb = B.stride(0) if k > 1 else max(n, 1)
+    ldc = out.stride(0) if m > 1 else max(n, 1)
+    ldr = (residual.stride(0) if m > 1 else max(n, 1)) if residual is not None else 0
+    ws = (None, 0) if workspace is None else _ws_args(workspace)
+    _check(lib().om_gemm_f32_ex(m, n, k, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc,
+                                _ptr_or_none(bias), _ptr_or_none(residual), ldr,
+                                ACTIVATIONS[activation], _mode(mode), ws[0], ws[1],
+                                _stream_handle(stream)), "om_gemm_f32_ex")
+    return out
+
+
+def conv2d_ex(x, w, stride: int = 1, padding: int = 0, dilation: int = 1, groups: int = 1,
+              bias=None, residual=None, activation=None, out=None, mode="exact", stream=None,
+              workspace=None, w_packed=None):
+    """act(conv2d(x, w) + bias[oc] + residual), NCHW. With w_packed given, w is
+    only used for its shape."""
+    import torch
+    _require(x, "x", 4)
+    args, yshape = _conv_geom(x, tuple(w.shape), stride, padding, dilation, groups)
+    if out is None:
+        out = torch.empty(yshape, dtype=torch.float32, device=x.device)
+    wsrc = w if w_packed is None else w_packed
+    ws = (None, 0) if workspace is None else _ws_args(workspace)
+    _check(lib().om_conv2d_f32_ex(*args, x.data_ptr(), wsrc.data_ptr(), int(w_packed is not None),
+                                  _ptr_or_none(bias), _ptr_or_none(residual),
+                                  ACTIVATIONS[activation], out.data_ptr(), _mode(mode), ws[0],
+                                  ws[1], _stream_handle(stream)), "om_conv2d_f32_ex")
+    return out

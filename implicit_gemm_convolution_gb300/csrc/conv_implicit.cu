@@ -49,6 +49,7 @@ struct ConvGeom {
     int KH, KW, sH, sW, pT, pL, dH, dW;
     int K, w_ld;
     int tiles_m, tiles_n, G;
+    Epilogue ep;
 };
 
 __device__ __forceinline__ void conv_record_timeout(int *abort_flag) {
@@ -211,13 +212,24 @@ __device__ __forceinline__ void conv_tile_io(const ConvGeom &g, Accum<Cfg> &acc,
                 acc.v[i][2 * q] = make_float2(e[0], e[1]);
                 acc.v[i][2 * q + 1] = make_float2(e[2], e[3]);
             } else {
-                const float4 v = (OP == 0) ? acc.out4(i, q)
-                                           : make_float4(acc.v[i][2 * q].x, acc.v[i][2 * q].y,
-                                                         acc.v[i][2 * q + 1].x, acc.v[i][2 * q + 1].y);
+                float e[4] = {acc.v[i][2 * q].x, acc.v[i][2 * q].y, acc.v[i][2 * q + 1].x,
+                              acc.v[i][2 * q + 1].y};
+                if constexpr (OP == 0) {
+                    const bool has_ep = g.ep.bias || g.ep.res || g.ep.act;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (has_ep && col + u < g.ncols) {
+                            const int64_t iu = (col + u) / g.P;
+                            const int64_t o = (iu * g.Cout + oc) * static_cast<int64_t>(g.P) + (col + u - iu * g.P);
+                            e[u] = epilogue_value(e[u], g.ep.bias ? g.ep.bias + oc : nullptr,
+                                                  g.ep.res ? g.ep.res + o : nullptr, g.ep.act);
+                        }
+                        e[u] = canonical_nan(e[u]);
+                    }
+                }
                 if (vec) {
-                    *reinterpret_cast<float4 *>(dst) = v;
+                    *reinterpret_cast<float4 *>(dst) = make_float4(e[0], e[1], e[2], e[3]);
                 } else {
-                    const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int64_t cu = col + u;
@@ -354,6 +366,7 @@ static cudaError_t launch_conv_cfg(const ConvProblem &p, unsigned *flags, cudaSt
     g.dH = static_cast<int>(p.dH); g.dW = static_cast<int>(p.dW);
     g.K = static_cast<int>(p.K); g.w_ld = static_cast<int>(p.w_ld);
     g.G = static_cast<int>(p.G);
+    g.ep = p.ep;
     const int64_t tiles_m = (g.M + Cfg::BM - 1) / Cfg::BM;
     const int64_t tiles_n = (g.ncols + Cfg::BN - 1) / Cfg::BN;
     if (tiles_m * tiles_n * p.G > 0x7FFFFFFF || p.w_ld > 0x7FFFFFFF) return cudaErrorNotSupported;

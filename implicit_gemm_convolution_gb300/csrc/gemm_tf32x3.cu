@@ -363,11 +363,17 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
                         const int64_t col = col0 + 4 * v;
-                        float4 o;
-                        o.x = canonical_nan(__uint_as_float(r[4 * v + 0]));
-                        o.y = canonical_nan(__uint_as_float(r[4 * v + 1]));
-                        o.z = canonical_nan(__uint_as_float(r[4 * v + 2]));
-                        o.w = canonical_nan(__uint_as_float(r[4 * v + 3]));
+                        float e[4] = {__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if ((p.ep.bias || p.ep.res || p.ep.act) && col + u < p.n)
+                                e[u] = epilogue_value(e[u], p.ep.bias ? p.ep.bias + col + u : nullptr,
+                                                      p.ep.res ? p.ep.res + row * p.ep.ldr + col + u : nullptr,
+                                                      p.ep.act);
+                            e[u] = canonical_nan(e[u]);
+                        }
+                        const float4 o = make_float4(e[0], e[1], e[2], e[3]);
                         if (vec_store && col + 3 < p.n) {
                             *reinterpret_cast<float4 *>(crow + col) = o;
                         } else {

@@ -170,7 +170,7 @@ Range ws_range(const unsigned *flags) { return span(flags, flags ? om::kMaxSched
 
 int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, const float *B,
               int64_t ldb, float *C, int64_t ldc, int mode, void *workspace, size_t ws_bytes,
-              void *stream) {
+              void *stream, const om::Epilogue &ep = om::Epilogue{}) {
     if (m < 0 || n < 0 || k < 0) return OM_ERR_INVALID_ARG;
     if (mode != OM_MODE_EXACT && mode != OM_MODE_FAST && mode != OM_MODE_TF32X3)
         return OM_ERR_UNSUPPORTED;
@@ -191,8 +191,22 @@ int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, cons
     const Range rw = ws_range(flags);
     if (flags && (overlaps(rw, rc) || (used && (overlaps(rw, ra) || overlaps(rw, rb)))))
         return OM_ERR_ALIAS;
+    // Epilogue operands: read only, never overlapping C or the workspace.
+    if (ep.act != 0 && ep.act != 1) return OM_ERR_INVALID_ARG;
+    if (ep.bias) {
+        if (!aligned4(ep.bias)) return OM_ERR_ALIGNMENT;
+        const Range rbias = span(ep.bias, n);
+        if (overlaps(rbias, rc) || (flags && overlaps(rbias, rw))) return OM_ERR_ALIAS;
+    }
+    if (ep.res) {
+        if (!aligned4(ep.res)) return OM_ERR_ALIGNMENT;
+        if (ep.ldr < n) return OM_ERR_INVALID_ARG;
+        Range rres;
+        if (!block_range(ep.res, m, n, ep.ldr, &rres)) return OM_ERR_TOO_LARGE;
+        if (overlaps(rres, rc) || (flags && overlaps(rres, rw))) return OM_ERR_ALIAS;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc};
+    GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc, ep};
     if (mode == OM_MODE_TF32X3) {
         if (k == 0) return from_cuda(om::launch_gemm_naive(p, OM_MODE_EXACT, s));  // +0
         cudaError_t e = om::launch_gemm_tf32x3(p, s);
@@ -213,21 +227,35 @@ int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, cons
 }
 
 int conv_impl(const ConvArgs &a, const float *x, const float *w, bool packed, float *y, int mode,
-              void *workspace, size_t ws_bytes, void *stream) {
+              void *workspace, size_t ws_bytes, void *stream,
+              const om::Epilogue &ep = om::Epilogue{}) {
     unsigned *flags = nullptr;
     const int wst = check_workspace(workspace, ws_bytes, &flags);
     if (wst != OM_OK) return wst;
+    if (ep.act != 0 && ep.act != 1) return OM_ERR_INVALID_ARG;
     ConvProblem p;
     bool empty = false;
     const int st = validate_conv(a, x, w, packed, y, mode, &p, &empty);
     if (st != OM_OK || empty) return st;
+    const Range rw = ws_range(flags);
+    const Range ry = span(y, static_cast<__int128>(p.N) * p.Cout * p.OH * p.OW);
     if (flags) {
-        const Range rw = ws_range(flags);
-        const Range ry = span(y, static_cast<__int128>(p.N) * p.Cout * p.OH * p.OW);
         const Range rx = span(x, static_cast<__int128>(p.N) * p.Cin * p.H * p.W);
         const Range rwt = span(w, static_cast<__int128>(p.Cout) * p.w_ld);
         if (overlaps(rw, ry) || overlaps(rw, rx) || overlaps(rw, rwt)) return OM_ERR_ALIAS;
     }
+    // Epilogue operands: read only, never overlapping y or the workspace.
+    if (ep.bias) {
+        if (!aligned4(ep.bias)) return OM_ERR_ALIGNMENT;
+        const Range rb = span(ep.bias, p.Cout);
+        if (overlaps(rb, ry) || (flags && overlaps(rb, rw))) return OM_ERR_ALIAS;
+    }
+    if (ep.res) {
+        if (!aligned4(ep.res)) return OM_ERR_ALIGNMENT;
+        const Range rr = span(ep.res, static_cast<__int128>(p.N) * p.Cout * p.OH * p.OW);
+        if (overlaps(rr, ry) || (flags && overlaps(rr, rw))) return OM_ERR_ALIAS;
+    }
+    p.ep = ep;
     return run_conv(p, mode, flags, static_cast<cudaStream_t>(stream));
 }
 
@@ -344,6 +372,24 @@ int om_conv2d_f32_packed_ws(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_
     if (!workspace) return OM_ERR_NULL_PTR;
     const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
     return conv_impl(a, x, w_packed, true, y, mode, workspace, workspace_bytes, stream);
+}
+
+int om_gemm_f32_ex(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda,
+                   const float *B, int64_t ldb, float *C, int64_t ldc, const float *bias,
+                   const float *residual, int64_t ldr, int activation, int mode, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+    const om::Epilogue ep{bias, residual, ldr, activation};
+    return gemm_impl(m, n, k, A, lda, B, ldb, C, ldc, mode, workspace, workspace_bytes, stream, ep);
+}
+
+int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout, int64_t G,
+                     int64_t KH, int64_t KW, int64_t stride, int64_t pad, int64_t dil,
+                     const float *x, const float *w, int weights_packed, const float *bias,
+                     const float *residual, int activation, float *y, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    const ConvArgs a{N, Cin, H, W, Cout, G, KH, KW, stride, pad, dil};
+    const om::Epilogue ep{bias, residual, 0, activation};
+    return conv_impl(a, x, w, weights_packed != 0, y, mode, workspace, workspace_bytes, stream, ep);
 }
 
 int om_device_status(void *stream) {

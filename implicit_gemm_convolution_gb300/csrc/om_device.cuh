@@ -30,6 +30,16 @@ __device__ __forceinline__ float canonical_nan(float v) {
     return (v != v) ? __int_as_float(0x7FC00000) : v;
 }
 
+// The output epilogue's arithmetic, one binary32 operation per step:
+// bias, then residual, then ReLU (keeps NaN, maps -0 and negatives to +0).
+__device__ __forceinline__ float epilogue_value(float v, const float *bias, const float *res,
+                                                int act) {
+    if (bias) v = __fadd_rn(v, *bias);
+    if (res) v = __fadd_rn(v, __ldg(res));
+    if (act == 1 && !(v > 0.0f) && v == v) v = 0.0f;
+    return v;
+}
+
 template <int MODE>
 __device__ __forceinline__ float term(float acc, float a, float b) {
     if constexpr (MODE == kFast) {

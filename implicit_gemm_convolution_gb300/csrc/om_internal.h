@@ -7,6 +7,18 @@
 
 namespace om {
 
+// Output epilogue, applied to each finished output before its NaN is made
+// canonical: v = v + bias[channel]; v = v + residual; v = relu(v). Every
+// pointer may be NULL (step skipped); act 0 = none, 1 = ReLU. For a product
+// the bias is per column and the residual has row stride ldr; for a
+// convolution the bias is per output channel and the residual has y's layout.
+struct Epilogue {
+    const float *bias;
+    const float *res;
+    int64_t ldr;
+    int act;
+};
+
 // A validated row-major product problem (device pointers).
 struct GemmProblem {
     int64_t m, n, k;
@@ -16,6 +28,7 @@ struct GemmProblem {
     int64_t ldb;
     float *C;
     int64_t ldc;
+    Epilogue ep;
 };
 
 // A validated convolution problem. Weights are read as the matrix
@@ -30,6 +43,7 @@ struct ConvProblem {
     const float *x;
     const float *w;
     float *y;
+    Epilogue ep;
 };
 
 // Kernel configurations the dispatcher can choose. A test-only environment

@@ -167,9 +167,25 @@ __device__ __forceinline__ void tile_io(const GemmProblem &p, Accum<Cfg> &acc, i
                 acc.v[i][2 * q] = make_float2(v.x, v.y);
                 acc.v[i][2 * q + 1] = make_float2(v.z, v.w);
             } else {
-                const float4 v = (OP == 0) ? acc.out4(i, q)
-                                           : make_float4(acc.v[i][2 * q].x, acc.v[i][2 * q].y,
-                                                         acc.v[i][2 * q + 1].x, acc.v[i][2 * q + 1].y);
+                float4 v = make_float4(acc.v[i][2 * q].x, acc.v[i][2 * q].y, acc.v[i][2 * q + 1].x,
+                                       acc.v[i][2 * q + 1].y);
+                if constexpr (OP == 0) {
+                    if (p.ep.bias || p.ep.res || p.ep.act) {
+                        float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (col + u < p.n)
+                                e[u] = epilogue_value(e[u], p.ep.bias ? p.ep.bias + col + u : nullptr,
+                                                      p.ep.res ? p.ep.res + row * p.ep.ldr + col + u : nullptr,
+                                                      p.ep.act);
+                        }
+                        v = make_float4(e[0], e[1], e[2], e[3]);
+                    }
+                    v.x = canonical_nan(v.x);
+                    v.y = canonical_nan(v.y);
+                    v.z = canonical_nan(v.z);
+                    v.w = canonical_nan(v.w);
+                }
                 if (vec) {
                     *reinterpret_cast<float4 *>(crow + col) = v;
                 } else {

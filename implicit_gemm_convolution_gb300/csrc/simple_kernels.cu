@@ -22,6 +22,9 @@ __global__ void gemm_naive_kernel(GemmProblem p) {
         for (int64_t q = 0; q < p.k; ++q) {
             acc = term<MODE>(acc, a[q], b[q * p.ldb]);
         }
+        if (p.ep.bias || p.ep.res || p.ep.act)
+            acc = epilogue_value(acc, p.ep.bias ? p.ep.bias + j : nullptr,
+                                 p.ep.res ? p.ep.res + i * p.ep.ldr + j : nullptr, p.ep.act);
         p.C[i * p.ldc + j] = canonical_nan(acc);
     }
 }
@@ -64,6 +67,9 @@ __global__ void conv_naive_kernel(ConvProblem p) {
                 }
             }
         }
+        if (p.ep.bias || p.ep.res || p.ep.act)
+            acc = epilogue_value(acc, p.ep.bias ? p.ep.bias + oc : nullptr,
+                                 p.ep.res ? p.ep.res + o : nullptr, p.ep.act);
         p.y[o] = canonical_nan(acc);
     }
 }

@@ -76,6 +76,11 @@ typedef enum om_mode {
     OM_MODE_TF32X3 = 2  /* tensor-core 3xTF32 split; tolerance, not bit-exact */
 } om_mode;
 
+typedef enum om_activation {
+    OM_ACT_NONE = 0,
+    OM_ACT_RELU = 1  /* max(v, +0); NaN stays NaN, -0 becomes +0 */
+} om_activation;
+
 /* Library version, OM_VERSION of the build. */
 OM_API int om_version(void);
 
@@ -253,6 +258,47 @@ OM_API int om_conv2d_f32_packed_ws(int64_t N, int64_t Cin, int64_t H, int64_t W,
                                    const float *x, const float *w_packed, float *y,
                                    int mode, void *workspace, size_t workspace_bytes,
                                    void *stream);
+
+/*
+ * Product with a fused output epilogue ("Convolution (fast mode)", sections
+ * "Tiles and chunks" -- bias, then activation, on each finished tile -- and
+ * "Single-column products" -- the bias, activation and residual epilogue).
+ * Each output v of the product is finished as
+ *   v = v + bias[j];  v = v + residual[i*ldr + j];  v = relu(v)
+ * one binary32 round-to-nearest operation per step (bias and residual are
+ * skipped when NULL; the pages do not fix the place of the residual, this
+ * library adds it before the activation, as a residual block needs), then a
+ * NaN is stored as 0x7FC00000. bias has n entries (one per column); residual
+ * is m x n with row stride ldr >= n and must not overlap C.
+ * activation: OM_ACT_NONE or OM_ACT_RELU. workspace may be NULL (the plain
+ * schedule) or a workspace as for om_gemm_f32_ws. Modes and errors as
+ * om_gemm_f32 / om_gemm_f32_ws; OM_ERR_INVALID_ARG for an unknown activation
+ * or a short ldr, OM_ERR_ALIAS for a residual or bias overlapping C.
+ */
+OM_API int om_gemm_f32_ex(int64_t m, int64_t n, int64_t k,
+                          const float *A, int64_t lda,
+                          const float *B, int64_t ldb,
+                          float *C, int64_t ldc,
+                          const float *bias, const float *residual, int64_t ldr, int activation,
+                          int mode, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Convolution with a fused output epilogue: output (n, oc, oy, ox) is
+ * finished as v + bias[oc], then + residual[n][oc][oy][ox], then the
+ * activation, as om_gemm_f32_ex. bias has Cout entries; residual has y's
+ * shape and must not overlap y. weights_packed != 0 takes w as laid out by
+ * om_pack_conv_weights. workspace may be NULL or a workspace as for
+ * om_conv2d_f32_ws. Errors as om_conv2d_f32 / om_conv2d_f32_ws, plus
+ * OM_ERR_INVALID_ARG for an unknown activation and OM_ERR_ALIAS for a
+ * residual or bias overlapping y.
+ */
+OM_API int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W,
+                            int64_t Cout, int64_t G, int64_t KH, int64_t KW,
+                            int64_t stride, int64_t pad, int64_t dil,
+                            const float *x, const float *w, int weights_packed,
+                            const float *bias, const float *residual, int activation,
+                            float *y, int mode, void *workspace, size_t workspace_bytes,
+                            void *stream);
 
 /*
  * Synchronises stream, then reads and clears the library's device status

@@ -129,3 +129,17 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(om, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         om.lib()
+
+
+def test_epilogue_entry_points_validate_on_host(L):
+    # unknown activation, residual aliasing the output, short residual stride
+    assert L.om_gemm_f32_ex(4, 4, 4, P, 4, P * 16, 4, P * 256, 4, None, None, 0, 5, 0, None, 0,
+                            None) == INV
+    assert L.om_gemm_f32_ex(4, 4, 4, P, 4, P * 16, 4, P * 256, 4, None, P * 256, 4, 1, 0, None, 0,
+                            None) == ALIAS
+    assert L.om_gemm_f32_ex(4, 4, 4, P, 4, P * 16, 4, P * 256, 4, None, P * 512, 2, 1, 0, None, 0,
+                            None) == INV
+    assert L.om_conv2d_f32_ex(1, 4, 5, 5, 4, 1, 3, 3, 1, 1, 1, P, P * 64, 0, None, None, 9,
+                              P * 256, 0, None, 0, None) == INV
+    assert L.om_conv2d_f32_ex(1, 4, 5, 5, 4, 1, 3, 3, 1, 1, 1, P, P * 64, 0, None, P * 256, 1,
+                              P * 256, 0, None, 0, None) == ALIAS
