@@ -34,8 +34,11 @@ namespace om {
 
 __device__ unsigned g_status_conv;
 
-// Registers of a producer thread (the gather keeps per-column state).
-constexpr int CONV_PRODUCER_REGS = 72;
+// The gather runs on one producer warpgroup, each thread keeping its
+// columns' state in registers; copying A with cp.async as well needs more.
+constexpr int kConvProducers = 128;
+template <bool A_TMA>
+constexpr int kConvProducerRegs = A_TMA ? 72 : 88;
 
 // Geometry the kernel reads (all per-image quantities fit in 32 bits; the
 // host validated Cin*H*W, Cout*OH*OW and K below 2^31).
@@ -67,17 +70,27 @@ __device__ __forceinline__ void conv_tile(const ConvGeom &g, int t, int &tm, int
     grp = r / g.tiles_n;
 }
 
-template <class Cfg, bool A_TMA>
+// Gather kinds: the general per-element gather, the masked gather for
+// kernels of up to 32 taps per channel, and the in-place copy of a 1x1,
+// stride-1, unpadded convolution (B is the input planes themselves; four
+// consecutive pixels of one channel per 16-byte copy).
+enum GatherKind : int { kGatherGeneral = 0, kGatherMasked = 1, kGather1x1 = 2 };
+
+template <class Cfg, bool A_TMA, int GATHER>
 __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMap *mapW,
                                              uint8_t *smem, uint64_t *full, uint64_t *empty,
                                              int *abort_flag, const Schedule &sched, int pt) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
-    constexpr int CPT = BN / kProducerThreads;  // gathered columns per producer thread
-    static_assert(BN % kProducerThreads == 0, "columns split evenly over the producer");
+    constexpr int CPT = BN / kConvProducers;  // gathered columns per producer thread
+    static_assert(BN % kConvProducers == 0, "columns split evenly over the producers");
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
     const int taps_per_channel = g.KH * g.KW;
+    constexpr bool MASKED = GATHER == kGatherMasked;
+    // tap-offset steps at the end of a kernel row and of a channel
+    const int64_t row_step = static_cast<int64_t>(g.dH) * g.W - static_cast<int64_t>(g.KW) * g.dW;
+    const int64_t chan_step = static_cast<int64_t>(g.HW) - static_cast<int64_t>(g.KH) * g.dH * g.W;
     const Schedule::Local L = sched.local();
     for (int si = 0; si < L.count; ++si) {
         const Segment sg = sched.at(L, si);
@@ -91,7 +104,7 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
         bool cvalid[CPT];
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
-            const int64_t col = tn * BN + pt + kProducerThreads * j;
+            const int64_t col = tn * BN + pt + kConvProducers * j;
             cvalid[j] = col < g.ncols;
             const int64_t img = cvalid[j] ? col / g.P : 0;
             const int pix = cvalid[j] ? static_cast<int>(col - img * g.P) : 0;
@@ -106,6 +119,30 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
         int c = p0 / taps_per_channel;
         int ky = (p0 - c * taps_per_channel) / g.KW;
         int kx = p0 - c * taps_per_channel - ky * g.KW;
+        int t = ky * g.KW + kx;
+        int64_t tapoff = static_cast<int64_t>(c) * g.HW + static_cast<int64_t>(ky) * g.dH * g.W +
+                         static_cast<int64_t>(kx) * g.dW;
+        // Masked gather (kernels of up to 32 taps per channel): per column the
+        // offset of its tap-(0,0) position and which taps lie in the plane.
+        uint32_t mask[CPT];
+        int64_t coloff[CPT];
+        if constexpr (MASKED) {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                coloff[j] = (base[j] - g.x) + static_cast<int64_t>(iy0[j]) * g.W + ix0[j];
+                uint32_t mk = 0;
+                if (cvalid[j]) {
+                    for (int y = 0; y < g.KH; ++y) {
+                        const bool yok = static_cast<unsigned>(iy0[j] + y * g.dH) < static_cast<unsigned>(g.H);
+                        for (int x = 0; x < g.KW; ++x) {
+                            const bool xok = static_cast<unsigned>(ix0[j] + x * g.dW) < static_cast<unsigned>(g.W);
+                            if (yok && xok) mk |= 1u << (y * g.KW + x);
+                        }
+                    }
+                }
+                mask[j] = mk;
+            }
+        }
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
                 conv_record_timeout(abort_flag);
@@ -134,7 +171,7 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
                 // rows of this group only; +0 past the group's rows and past K
                 const int kk = pt % 32;
                 const int p = kt * BK + kk;
-                for (int r = pt / 32; r < BM; r += 4) {
+                for (int r = pt / 32; r < BM; r += kConvProducers / 32) {
                     const int mrow = tm * BM + r;
                     const bool ok = (mrow < g.M) && (p < g.K);
                     const float *src = ok ? g.w + static_cast<int64_t>(row0 + r) * g.w_ld + p : g.w;
@@ -142,25 +179,70 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
                 }
             }
             // Gather the 32 taps of this stage for the thread's columns.
+            if constexpr (GATHER == kGather1x1) {
+                // thread pt copies pixels 4*(pt % 64) .. +3 of the tile for the
+                // channels of parity pt / 64; each group of four is one image
+                // (OH*OW is a multiple of 4) and 16-byte aligned
+                const int q = pt % (BN / 4);
+                const int64_t col = tn * BN + 4 * q;
+                const bool col_ok = col < g.ncols;
+                const int64_t img = col_ok ? col / g.P : 0;
+                const int64_t pix = col - img * g.P;
+                const float *cbase = g.x + (img * g.Cin + static_cast<int64_t>(grp) * g.cin_g) * g.HW + pix;
+                constexpr int kRowsPerPass = kConvProducers / (BN / 4);
 #pragma unroll 4
-            for (int kk = 0; kk < BK; ++kk) {
-                const int p = kt * BK + kk;
-                const bool tap_ok = p < g.K;
-                const int dy = ky * g.dH, dx = kx * g.dW;
-                const int plane = tap_ok ? c * g.HW : 0;
-#pragma unroll
-                for (int j = 0; j < CPT; ++j) {
-                    const int iy = iy0[j] + dy, ix = ix0[j] + dx;
-                    const bool ok = tap_ok && cvalid[j] && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
-                                    static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
-                    const float *src = ok ? base[j] + (plane + iy * g.W + ix) : g.x;
-                    cp_async_4(sb32 + (kk * BN + pt + kProducerThreads * j) * 4, src, ok ? 4u : 0u);
+                for (int kk = pt / (BN / 4); kk < BK; kk += kRowsPerPass) {
+                    const int ch = kt * BK + kk;
+                    const bool ok = col_ok && ch < g.K;
+                    const float *src = ok ? cbase + static_cast<int64_t>(ch) * g.HW : g.x;
+                    cp_async_16(sb32 + (kk * BN + 4 * q) * 4, src, ok ? 16u : 0u);
                 }
-                if (++kx == g.KW) {
-                    kx = 0;
-                    if (++ky == g.KH) {
-                        ky = 0;
-                        ++c;
+            } else if constexpr (MASKED) {
+                // tap t of a channel is in the plane for column j iff bit t of
+                // mask[j] is set; tapoff is the tap's offset from the column's
+                // tap-(0,0) position (c*H*W + ky*dH*W + kx*dW)
+#pragma unroll 4
+                for (int kk = 0; kk < BK; ++kk) {
+                    const bool tap_ok = kt * BK + kk < g.K;
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) {
+                        const bool ok = tap_ok && ((mask[j] >> t) & 1u);
+                        const float *src = ok ? g.x + (coloff[j] + tapoff) : g.x;
+                        cp_async_4(sb32 + (kk * BN + pt + kConvProducers * j) * 4, src, ok ? 4u : 0u);
+                    }
+                    tapoff += g.dW;
+                    ++t;
+                    if (++kx == g.KW) {
+                        kx = 0;
+                        tapoff += row_step;
+                        if (++ky == g.KH) {
+                            ky = 0;
+                            t = 0;
+                            tapoff += chan_step;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 4
+                for (int kk = 0; kk < BK; ++kk) {
+                    const int p = kt * BK + kk;
+                    const bool tap_ok = p < g.K;
+                    const int dy = ky * g.dH, dx = kx * g.dW;
+                    const int plane = tap_ok ? c * g.HW : 0;
+#pragma unroll
+                    for (int j = 0; j < CPT; ++j) {
+                        const int iy = iy0[j] + dy, ix = ix0[j] + dx;
+                        const bool ok = tap_ok && cvalid[j] && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
+                                        static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
+                        const float *src = ok ? base[j] + (plane + iy * g.W + ix) : g.x;
+                        cp_async_4(sb32 + (kk * BN + pt + kConvProducers * j) * 4, src, ok ? 4u : 0u);
+                    }
+                    if (++kx == g.KW) {
+                        kx = 0;
+                        if (++ky == g.KH) {
+                            ky = 0;
+                            ++c;
+                        }
                     }
                 }
             }
@@ -178,7 +260,7 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
 // the tile is output channel grp*M + tm*BM + i; column j is (image, pixel) =
 // divmod(j, OH*OW). OP 0: final store (canonical NaN); 1: raw store of an
 // early part's accumulators; 2: load of the accumulators an earlier CTA stored.
-template <class Cfg, int OP>
+template <class Cfg, int OP, bool HAS_EP>
 __device__ __forceinline__ void conv_tile_io(const ConvGeom &g, Accum<Cfg> &acc, int tm,
                                              int64_t tn, int grp, int arow0, int bcol0) {
     const bool vec_ok = (g.P % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.y) & 15) == 0);
@@ -214,20 +296,18 @@ __device__ __forceinline__ void conv_tile_io(const ConvGeom &g, Accum<Cfg> &acc,
             } else {
                 float e[4] = {acc.v[i][2 * q].x, acc.v[i][2 * q].y, acc.v[i][2 * q + 1].x,
                               acc.v[i][2 * q + 1].y};
-                if constexpr (OP == 0) {
-                    const bool has_ep = g.ep.bias || g.ep.res || g.ep.act;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        if (has_ep && col + u < g.ncols) {
-                            const int64_t iu = (col + u) / g.P;
-                            const int64_t o = (iu * g.Cout + oc) * static_cast<int64_t>(g.P) + (col + u - iu * g.P);
-                            e[u] = epilogue_value(e[u], g.ep.bias ? g.ep.bias + oc : nullptr,
-                                                  g.ep.res ? g.ep.res + o : nullptr, g.ep.act);
-                        }
-                        e[u] = canonical_nan(e[u]);
-                    }
-                }
                 if (vec) {
+                    // four columns of one image: consecutive outputs from dst
+                    if constexpr (OP == 0) {
+                        const int64_t o = dst - g.y;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (HAS_EP)
+                                e[u] = epilogue_value(e[u], g.ep.bias ? g.ep.bias + oc : nullptr,
+                                                      g.ep.res ? g.ep.res + o + u : nullptr, g.ep.act);
+                            e[u] = canonical_nan(e[u]);
+                        }
+                    }
                     *reinterpret_cast<float4 *>(dst) = make_float4(e[0], e[1], e[2], e[3]);
                 } else {
 #pragma unroll
@@ -235,7 +315,15 @@ __device__ __forceinline__ void conv_tile_io(const ConvGeom &g, Accum<Cfg> &acc,
                         const int64_t cu = col + u;
                         if (cu >= g.ncols) break;
                         const int64_t iu = cu / g.P;
-                        g.y[(iu * g.Cout + oc) * static_cast<int64_t>(g.P) + (cu - iu * g.P)] = e[u];
+                        const int64_t o = (iu * g.Cout + oc) * static_cast<int64_t>(g.P) + (cu - iu * g.P);
+                        float v = e[u];
+                        if constexpr (OP == 0) {
+                            if (HAS_EP)
+                                v = epilogue_value(v, g.ep.bias ? g.ep.bias + oc : nullptr,
+                                                   g.ep.res ? g.ep.res + o : nullptr, g.ep.act);
+                            v = canonical_nan(v);
+                        }
+                        g.y[o] = v;
                     }
                 }
             }
@@ -243,8 +331,8 @@ __device__ __forceinline__ void conv_tile_io(const ConvGeom &g, Accum<Cfg> &acc,
     }
 }
 
-template <int MODE, class Cfg, bool A_TMA>
-__global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
+template <int MODE, class Cfg, bool A_TMA, bool HAS_EP, int GATHER>
+__global__ void __launch_bounds__(Cfg::CONSUMERS + kConvProducers, 1)
     conv_implicit_kernel(const __grid_constant__ CUtensorMap mapW, ConvGeom g, Schedule sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = aligned_smem<Cfg>(smem_raw);
@@ -256,7 +344,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
         for (int s = 0; s < Cfg::STAGES; ++s) {
             // every producer thread arrives after its copies land; with TMA
             // weights, producer thread 0 also arrives with the byte count
-            mbar_init(&full[s], kProducerThreads + (A_TMA ? 1 : 0));
+            mbar_init(&full[s], kConvProducers + (A_TMA ? 1 : 0));
             mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
         }
         *abort_flag = 0;
@@ -266,16 +354,16 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     __syncthreads();
 
     if (warp >= Cfg::CONSUMER_WARPS) {
-        RegSplit<CONV_PRODUCER_REGS>::producer();
+        RegSplit<kConvProducerRegs<A_TMA>, kConvProducers, Cfg::CONSUMERS>::producer();
         if constexpr (A_TMA) {
             if (threadIdx.x == Cfg::CONSUMERS) prefetch_tensormap(&mapW);
         }
-        conv_produce<Cfg, A_TMA>(g, &mapW, smem, full, empty, abort_flag, sched,
+        conv_produce<Cfg, A_TMA, GATHER>(g, &mapW, smem, full, empty, abort_flag, sched,
                                  threadIdx.x - Cfg::CONSUMERS);
         return;
     }
 
-    RegSplit<CONV_PRODUCER_REGS>::consumer();
+    RegSplit<kConvProducerRegs<A_TMA>, kConvProducers, Cfg::CONSUMERS>::consumer();
     const int ty = lane / 4, tx = lane % 4;
     const int arow0 = (warp / Cfg::WARPS_N) * Cfg::WM + ty;
     const int bcol0 = (warp % Cfg::WARPS_N) * Cfg::WN + tx * 4;
@@ -294,7 +382,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
                 atomicOr(&g_status_conv, kDevErrTimeout);
                 return;
             }
-            conv_tile_io<Cfg, 2>(g, acc, tm, tn, grp, arow0, bcol0);
+            conv_tile_io<Cfg, 2, false>(g, acc, tm, tn, grp, arow0, bcol0);
         }
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&full[stage], phase)) {
@@ -312,10 +400,10 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
             }
         }
         if (sg.kind == kSegEarly) {
-            conv_tile_io<Cfg, 1>(g, acc, tm, tn, grp, arow0, bcol0);
+            conv_tile_io<Cfg, 1, false>(g, acc, tm, tn, grp, arow0, bcol0);
             signal_early_part(sched.flags, Cfg::CONSUMERS);
         } else {
-            conv_tile_io<Cfg, 0>(g, acc, tm, tn, grp, arow0, bcol0);
+            conv_tile_io<Cfg, 0, HAS_EP>(g, acc, tm, tn, grp, arow0, bcol0);
         }
     }
 }
@@ -380,21 +468,44 @@ static cudaError_t launch_conv_cfg(const ConvProblem &p, unsigned *flags, cudaSt
     memset(&map, 0, sizeof(map));
     const bool a_tma = ((reinterpret_cast<uintptr_t>(p.w) & 15) == 0) && (p.w_ld % 4 == 0) &&
                        make_weight_map(&map, p, Cfg::BM);
-    void (*kernel)(const CUtensorMap, ConvGeom, Schedule) =
-        a_tma ? conv_implicit_kernel<MODE, Cfg, true> : conv_implicit_kernel<MODE, Cfg, false>;
+    const bool has_ep = p.ep.bias || p.ep.res || p.ep.act;
+    // 1x1, stride 1, no padding, pixel counts multiples of 4, 16-byte aligned
+    // input: B is the input planes, copied 16 bytes at a time
+    const bool in_place = p.KH == 1 && p.KW == 1 && p.sH == 1 && p.sW == 1 && p.pT == 0 &&
+                          p.pL == 0 && (p.OH * p.OW) % 4 == 0 && (p.H * p.W) % 4 == 0 &&
+                          (reinterpret_cast<uintptr_t>(p.x) & 15) == 0;
+    const int gather = in_place ? kGather1x1 : (p.KH * p.KW <= 32 ? kGatherMasked : kGatherGeneral);
+    void (*kernel)(const CUtensorMap, ConvGeom, Schedule) = nullptr;
+#define OM_CONV_PICK(T, E, G) \
+    if (a_tma == T && has_ep == E && gather == G) kernel = conv_implicit_kernel<MODE, Cfg, T, E, G>;
+#define OM_CONV_PICK_G(T, E)             \
+    OM_CONV_PICK(T, E, kGatherGeneral)   \
+    OM_CONV_PICK(T, E, kGatherMasked)    \
+    OM_CONV_PICK(T, E, kGather1x1)
+    OM_CONV_PICK_G(true, false)
+    OM_CONV_PICK_G(true, true)
+    OM_CONV_PICK_G(false, false)
+    OM_CONV_PICK_G(false, true)
+#undef OM_CONV_PICK_G
+#undef OM_CONV_PICK
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s,
+    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kConvProducers, Cfg::SMEM_BYTES, s,
                             map, g, sched);
 }
 
 cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, unsigned *flags,
                                  cudaStream_t s) {
-    if (cfg != kConvAuto && cfg != kConvImplicit) return cudaErrorNotSupported;
     if (p.K == 0) return cudaErrorNotSupported;
-    return mode == kFast ? launch_conv_cfg<kFast, ConvCfg64x256>(p, flags, s)
-                         : launch_conv_cfg<kExact, ConvCfg64x256>(p, flags, s);
+    if (cfg == kConvAuto) cfg = kConvImplicit;
+    switch (cfg) {
+        case kConvImplicit:
+            return mode == kFast ? launch_conv_cfg<kFast, ConvCfg64x256>(p, flags, s)
+                                 : launch_conv_cfg<kExact, ConvCfg64x256>(p, flags, s);
+        default:
+            return cudaErrorNotSupported;
+    }
 }
 
 cudaError_t read_clear_status_conv(unsigned *out, cudaStream_t s) {

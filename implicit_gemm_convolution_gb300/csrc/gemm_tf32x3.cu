@@ -13,7 +13,7 @@
 //
 // CTA (one per SM, persistent over 128 x 128 output tiles), 14 warps:
 //   warp 0      TMA producer: fp32 A tile 128 x 32 (128B swizzle, k
-//               innermost) and fp32 B tile 32 x 128 into a 2-stage ring.
+//               innermost) and fp32 B tile 32 x 128 into a 3-stage ring.
 //   warp 1      allocates 256 tensor-memory columns (two 128-column fp32
 //               accumulators), then one thread issues tcgen05.mma.
 //   warps 2-9   converters: split each fp32 stage into hi/lo tiles in the
@@ -38,7 +38,7 @@ __device__ unsigned g_status_tc;
 namespace tc {
 
 constexpr int BM = 128, BN = 128, BK = 32;  // BK fp32 = one 128-byte row
-constexpr int S_F32 = 2;                     // fp32 stages
+constexpr int S_F32 = 3;                     // fp32 stages
 constexpr int S_OPS = 2;                     // converted operand stages
 constexpr int TILE_BYTES = 128 * 32 * 4;     // 16 KB: any 128 x 32 fp32 tile
 constexpr int F32_STAGE = 2 * TILE_BYTES;    // A, B

@@ -189,6 +189,14 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
+// 16-byte copy global -> shared (both 16-byte aligned); src_bytes 0 or 16,
+// 0 writes +0 without reading.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 // Arrive on bar once every cp.async this thread issued so far has landed.
 // The barrier's expected count must include this arrival (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {

@@ -61,7 +61,7 @@ enum GemmCfg : int {
 enum ConvCfg : int {
     kConvAuto = -1,
     kConvNaive = 0,     // one thread per output, direct loops
-    kConvImplicit = 1,  // implicit GEMM with gathered patches
+    kConvImplicit = 1,  // implicit GEMM with gathered patches, 64 x 256 tiles
 };
 
 cudaError_t launch_gemm_naive(const GemmProblem &p, int mode, cudaStream_t s);

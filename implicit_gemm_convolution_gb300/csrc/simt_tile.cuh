@@ -49,24 +49,30 @@ struct TileCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzled tiles need 1 KB alignment");
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-    static_assert(CONSUMERS == 256, "the register split assumes two consumer warpgroups");
+    static_assert(CONSUMERS % 128 == 0, "consumers come in whole warpgroups");
 };
 
-// One producer warpgroup and two consumer warpgroups. Launched at
-// kLaunchRegs per thread, the producer warpgroup gives registers back
-// (setmaxnreg.dec) and the consumers take them (setmaxnreg.inc): a TMA
-// producer needs almost none, a gathering producer keeps per-column state.
-constexpr int kProducerThreads = 128;
-constexpr int kLaunchRegs = 168;
+// Producer warpgroup(s) and two consumer warpgroups. At launch every thread
+// gets the same registers (65536 / threads, rounded down to 8); the
+// producers give registers back (setmaxnreg.dec) and the consumers take them
+// (setmaxnreg.inc): a TMA producer needs almost none, a gathering producer
+// keeps per-column state.
+constexpr int kProducerThreads = 128;  // one producer warpgroup (the GEMM kernels)
+constexpr int kLaunchRegs = 168;       // 384 threads
 
-template <int PRODUCER_REGS>
+template <int PRODUCER_REGS, int PRODUCERS = 128, int CONSUMERS = 256>
 struct RegSplit {
+    static constexpr int kThreads = PRODUCERS + CONSUMERS;
+    static constexpr int kLaunch = (65536 / kThreads) / 8 * 8;
     static constexpr int kProducer = PRODUCER_REGS;
-    // what the producer gives back, shared by the 256 consumer threads
-    static constexpr int kConsumer = ((384 * kLaunchRegs - 128 * PRODUCER_REGS) / 256) / 8 * 8;
-    static_assert(kConsumer <= 256 && PRODUCER_REGS >= 24 && PRODUCER_REGS % 8 == 0,
+    static constexpr int kConsumer =
+        ((kThreads * kLaunch - PRODUCERS * PRODUCER_REGS) / CONSUMERS) / 8 * 8 > 256
+            ? 256
+            : ((kThreads * kLaunch - PRODUCERS * PRODUCER_REGS) / CONSUMERS) / 8 * 8;
+    static_assert(PRODUCERS % 128 == 0 && CONSUMERS % 128 == 0, "whole warpgroups");
+    static_assert(PRODUCER_REGS >= 24 && PRODUCER_REGS % 8 == 0 && PRODUCER_REGS <= kLaunch,
                   "setmaxnreg range");
-    static_assert(128 * kProducer + 256 * kConsumer <= 384 * kLaunchRegs,
+    static_assert(PRODUCERS * kProducer + CONSUMERS * kConsumer <= kThreads * kLaunch,
                   "register split exceeds the launch allocation");
     __device__ __forceinline__ static void producer() {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducer));

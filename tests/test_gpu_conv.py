@@ -69,6 +69,14 @@ SMALL = [
     (2, 40, 13, 11, 70, 1, 3, 3, 2, 1, 1),
     (1, 3, 30, 30, 16, 1, 7, 7, 2, 3, 1),
     (4, 64, 7, 7, 128, 1, 3, 3, 1, 1, 1),
+    # 1x1 stride 1 unpadded with pixel counts a multiple of 4 (the input
+    # planes are B, copied 16 bytes at a time): ragged channels and columns,
+    # images straddling column tiles
+    (2, 20, 6, 6, 24, 1, 1, 1, 1, 0, 1),
+    (5, 37, 12, 12, 40, 1, 1, 1, 1, 0, 1),
+    # 1x1 that must not take that copy: 25 pixels, stride 2
+    (2, 33, 5, 5, 8, 1, 1, 1, 1, 0, 1),
+    (2, 12, 8, 8, 16, 1, 1, 1, 2, 0, 1),
 ]
 
 
@@ -159,3 +167,22 @@ def test_workspace_odd_geometry(mode, name):
     want = want_conv(c, mode)
     for cfg in (None, 1):
         assert_bits_equal(run_conv(c, name, cfg, workspace=ws), want, f"odd ws cfg={cfg}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_1x1_input_not_16_byte_aligned(mode, name):
+    # the same 1x1 geometry with x starting 4 bytes past a 16-byte boundary
+    import torch
+    c = synth.make_conv("t", 3, 24, 8, 8, 32, 1, 1, 1, 1, 0, 1, seed=7,
+                        dist_x=("uniform", -1, 1), dist_w=("normal", 0, 0.5))
+    xbuf = torch.zeros(c.x.size + 4, dtype=torch.float32, device="cuda")
+    xbuf[1:1 + c.x.size] = to_dev(c.x).reshape(-1)
+    x = xbuf[1:1 + c.x.size]
+    assert x.data_ptr() % 16 == 4
+    w = to_dev(c.w)
+    y = torch.empty((c.N, c.Cout, c.H, c.W), device="cuda")
+    st = om.lib().om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, 1, 1, 1, 0, 1, x.data_ptr(),
+                                w.data_ptr(), y.data_ptr(), om.MODES[name], None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(y.cpu().numpy(), want_conv(c, mode), "misaligned 1x1")
