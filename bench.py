@@ -135,12 +135,25 @@ def gemm_workload():
     return synth.workload_gemm_4096()
 
 
-def kernel_source_hash() -> str:
+# The sources each kernel's translation unit is built from.
+KERNEL_SOURCES = {
+    "sgemm_tiled_kernel": ("sgemm_tiled.cu", "simt_tile.cuh", "om_device.cuh", "om_internal.h",
+                           "schedule_host.h"),
+    "conv_implicit_kernel": ("conv_implicit.cu", "simt_tile.cuh", "om_device.cuh", "om_internal.h",
+                             "schedule_host.h"),
+    "gemm_tf32x3_kernel": ("gemm_tf32x3.cu", "om_device.cuh", "om_internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str = "") -> str:
+    """SHA-256 prefix of the kernel's sources (all of csrc/ if the kernel is
+    not listed in KERNEL_SOURCES)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "implicit_gemm_convolution_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    files = KERNEL_SOURCES.get(kernel) or sorted(
+        f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -156,7 +169,7 @@ def recorded_traffic(kernel: str, workload: str):
     for line in lines:
         parts = line.split()
         if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
-            return int(parts[3]) if parts[2] == kernel_source_hash() else None
+            return int(parts[3]) if parts[2] == kernel_source_hash(kernel) else None
     return None
 
 

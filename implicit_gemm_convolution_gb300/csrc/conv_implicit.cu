@@ -70,16 +70,26 @@ __device__ __forceinline__ void conv_tile(const ConvGeom &g, int t, int &tm, int
     grp = r / g.tiles_n;
 }
 
-// Gather kinds: the general per-element gather, the masked gather for
-// kernels of up to 32 taps per channel, and the in-place copy of a 1x1,
-// stride-1, unpadded convolution (B is the input planes themselves; four
-// consecutive pixels of one channel per 16-byte copy).
+// Gather kinds: the general per-element gather; the masked gather (kernels
+// of up to 32 taps per channel, input below 2^31 elements, tap table in
+// shared memory); and the in-place copy of a 1x1, stride-1, unpadded
+// convolution (B is the input planes themselves; four consecutive pixels of
+// one channel per 16-byte copy).
 enum GatherKind : int { kGatherGeneral = 0, kGatherMasked = 1, kGather1x1 = 2 };
+
+// Shared-memory bytes of the masked gather's tap table: per tap p (padded
+// to whole k blocks) its input offset c*H*W + ky*dH*W + kx*dW and the bit
+// 1 << (ky*KW + kx), or 0 past K.
+template <class Cfg>
+inline int64_t conv_tap_table_bytes(int64_t K) {
+    return (K + Cfg::BK - 1) / Cfg::BK * Cfg::BK * 8;
+}
 
 template <class Cfg, bool A_TMA, int GATHER>
 __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMap *mapW,
                                              uint8_t *smem, uint64_t *full, uint64_t *empty,
-                                             int *abort_flag, const Schedule &sched, int pt) {
+                                             int *abort_flag, const Schedule &sched, int pt,
+                                             uint8_t *tap_table) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
     constexpr int CPT = BN / kConvProducers;  // gathered columns per producer thread
     static_assert(BN % kConvProducers == 0, "columns split evenly over the producers");
@@ -88,9 +98,18 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
     int64_t issued = 0;
     const int taps_per_channel = g.KH * g.KW;
     constexpr bool MASKED = GATHER == kGatherMasked;
-    // tap-offset steps at the end of a kernel row and of a channel
-    const int64_t row_step = static_cast<int64_t>(g.dH) * g.W - static_cast<int64_t>(g.KW) * g.dW;
-    const int64_t chan_step = static_cast<int64_t>(g.HW) - static_cast<int64_t>(g.KH) * g.dH * g.W;
+    const uint32_t tab32 = smem_u32(tap_table);
+    if constexpr (MASKED) {
+        const int kpad = (g.K + BK - 1) / BK * BK;
+        for (int p = pt; p < kpad; p += kConvProducers) {
+            const int c = p / taps_per_channel;
+            const int t = p - c * taps_per_channel;
+            const int ky = t / g.KW, kx = t - (t / g.KW) * g.KW;
+            const int off = c * g.HW + ky * g.dH * g.W + kx * g.dW;
+            reinterpret_cast<int2 *>(tap_table)[p] = make_int2(off, p < g.K ? static_cast<int>(1u << t) : 0);
+        }
+        asm volatile("bar.sync 2, %0;" ::"n"(kConvProducers) : "memory");
+    }
     const Schedule::Local L = sched.local();
     for (int si = 0; si < L.count; ++si) {
         const Segment sg = sched.at(L, si);
@@ -119,17 +138,15 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
         int c = p0 / taps_per_channel;
         int ky = (p0 - c * taps_per_channel) / g.KW;
         int kx = p0 - c * taps_per_channel - ky * g.KW;
-        int t = ky * g.KW + kx;
-        int64_t tapoff = static_cast<int64_t>(c) * g.HW + static_cast<int64_t>(ky) * g.dH * g.W +
-                         static_cast<int64_t>(kx) * g.dW;
-        // Masked gather (kernels of up to 32 taps per channel): per column the
-        // offset of its tap-(0,0) position and which taps lie in the plane.
+        // Masked gather: per column the offset of its tap-(0,0) position (an
+        // int: the input has fewer than 2^31 elements) and which taps lie in
+        // the plane.
         uint32_t mask[CPT];
-        int64_t coloff[CPT];
+        int coloff[CPT];
         if constexpr (MASKED) {
 #pragma unroll
             for (int j = 0; j < CPT; ++j) {
-                coloff[j] = (base[j] - g.x) + static_cast<int64_t>(iy0[j]) * g.W + ix0[j];
+                coloff[j] = static_cast<int>((base[j] - g.x) + static_cast<int64_t>(iy0[j]) * g.W + ix0[j]);
                 uint32_t mk = 0;
                 if (cvalid[j]) {
                     for (int y = 0; y < g.KH; ++y) {
@@ -198,28 +215,17 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
                     cp_async_16(sb32 + (kk * BN + 4 * q) * 4, src, ok ? 16u : 0u);
                 }
             } else if constexpr (MASKED) {
-                // tap t of a channel is in the plane for column j iff bit t of
-                // mask[j] is set; tapoff is the tap's offset from the column's
-                // tap-(0,0) position (c*H*W + ky*dH*W + kx*dW)
-#pragma unroll 4
+                // tap p is in the plane for column j iff mask[j] has the tap's
+                // bit; its input element is then coloff[j] + the tap's offset
+                const uint32_t trow = tab32 + kt * BK * 8;
+#pragma unroll 8
                 for (int kk = 0; kk < BK; ++kk) {
-                    const bool tap_ok = kt * BK + kk < g.K;
+                    const int2 e = lds_int2(trow + kk * 8);
 #pragma unroll
                     for (int j = 0; j < CPT; ++j) {
-                        const bool ok = tap_ok && ((mask[j] >> t) & 1u);
-                        const float *src = ok ? g.x + (coloff[j] + tapoff) : g.x;
-                        cp_async_4(sb32 + (kk * BN + pt + kConvProducers * j) * 4, src, ok ? 4u : 0u);
-                    }
-                    tapoff += g.dW;
-                    ++t;
-                    if (++kx == g.KW) {
-                        kx = 0;
-                        tapoff += row_step;
-                        if (++ky == g.KH) {
-                            ky = 0;
-                            t = 0;
-                            tapoff += chan_step;
-                        }
+                        const bool ok = (mask[j] & static_cast<uint32_t>(e.y)) != 0u;
+                        const int off = ok ? coloff[j] + e.x : 0;
+                        cp_async_4_if(sb32 + (kk * BN + pt + kConvProducers * j) * 4, g.x + off, ok);
                     }
                 }
             } else {
@@ -339,6 +345,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kConvProducers, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
     uint64_t *empty = full + Cfg::STAGES;
     int *abort_flag = reinterpret_cast<int *>(empty + Cfg::STAGES);
+    uint8_t *tap_table = smem + Cfg::STAGES * Cfg::STAGE_BYTES + 256;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kConvProducers, 1)
             if (threadIdx.x == Cfg::CONSUMERS) prefetch_tensormap(&mapW);
         }
         conv_produce<Cfg, A_TMA, GATHER>(g, &mapW, smem, full, empty, abort_flag, sched,
-                                 threadIdx.x - Cfg::CONSUMERS);
+                                         threadIdx.x - Cfg::CONSUMERS, tap_table);
         return;
     }
 
@@ -474,7 +481,11 @@ static cudaError_t launch_conv_cfg(const ConvProblem &p, unsigned *flags, cudaSt
     const bool in_place = p.KH == 1 && p.KW == 1 && p.sH == 1 && p.sW == 1 && p.pT == 0 &&
                           p.pL == 0 && (p.OH * p.OW) % 4 == 0 && (p.H * p.W) % 4 == 0 &&
                           (reinterpret_cast<uintptr_t>(p.x) & 15) == 0;
-    const int gather = in_place ? kGather1x1 : (p.KH * p.KW <= 32 ? kGatherMasked : kGatherGeneral);
+    const int64_t table_bytes = conv_tap_table_bytes<Cfg>(p.K);
+    const bool masked = p.KH * p.KW <= 32 && p.N * p.Cin * p.H * p.W <= 0x7FFFFFFF &&
+                        Cfg::SMEM_BYTES + table_bytes <= max_smem_optin();
+    const int gather = in_place ? kGather1x1 : (masked ? kGatherMasked : kGatherGeneral);
+    const int smem_bytes = Cfg::SMEM_BYTES + (gather == kGatherMasked ? static_cast<int>(table_bytes) : 0);
     void (*kernel)(const CUtensorMap, ConvGeom, Schedule) = nullptr;
 #define OM_CONV_PICK(T, E, G) \
     if (a_tma == T && has_ep == E && gather == G) kernel = conv_implicit_kernel<MODE, Cfg, T, E, G>;
@@ -489,10 +500,10 @@ static cudaError_t launch_conv_cfg(const ConvProblem &p, unsigned *flags, cudaSt
 #undef OM_CONV_PICK_G
 #undef OM_CONV_PICK
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               Cfg::SMEM_BYTES);
+                                               smem_bytes);
     if (e != cudaSuccess) return e;
-    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kConvProducers, Cfg::SMEM_BYTES, s,
-                            map, g, sched);
+    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kConvProducers, smem_bytes, s, map, g,
+                            sched);
 }
 
 cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, unsigned *flags,

@@ -22,6 +22,17 @@ int num_sms() {
     return v;
 }
 
+int max_smem_optin() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) v = 0;
+    if (dev < 64 && v > 0) cached[dev] = v;
+    return v;
+}
+
 }  // namespace om
 
 namespace {

@@ -189,6 +189,23 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 
+// 4-byte copy global -> shared when ok, else +0 written without reading src
+// (src must still be a valid address).
+__device__ __forceinline__ void cp_async_4_if(uint32_t dst, const void *src, bool ok) {
+    asm volatile(
+        "{\n\t.reg .pred skip;\n\tsetp.eq.u32 skip, %2, 0;\n\t"
+        "cp.async.ca.shared.global [%0], [%1], 4, skip;\n\t}" ::"r"(dst),
+        "l"(src), "r"(static_cast<uint32_t>(ok))
+        : "memory");
+}
+
+// Two 32-bit integers from shared memory.
+__device__ __forceinline__ int2 lds_int2(uint32_t a) {
+    int2 v;
+    asm volatile("ld.shared.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
 // 16-byte copy global -> shared (both 16-byte aligned); src_bytes 0 or 16,
 // 0 writes +0 without reading.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {

@@ -94,6 +94,8 @@ int gemm_with_scratch(int64_t m, int64_t n, int64_t k, const float *A, int64_t l
 cudaError_t read_clear_status_gemm(unsigned *out, cudaStream_t s);
 cudaError_t read_clear_status_conv(unsigned *out, cudaStream_t s);
 
+// Largest dynamic shared memory a block may opt in to on the current device.
+int max_smem_optin();
 int num_sms();
 
 // Largest grid the balanced schedule runs (one flag word per CTA).

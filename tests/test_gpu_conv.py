@@ -77,6 +77,9 @@ SMALL = [
     # 1x1 that must not take that copy: 25 pixels, stride 2
     (2, 33, 5, 5, 8, 1, 1, 1, 1, 0, 1),
     (2, 12, 8, 8, 16, 1, 1, 1, 2, 0, 1),
+    # K = 9216 taps: the tap table would not fit in shared memory beside the
+    # stages, so the per-element gather runs
+    (1, 1024, 6, 5, 8, 1, 3, 3, 1, 1, 1),
 ]
 
 
