@@ -1,0 +1,274 @@
+// Direct convolution for groups with few output channels: depthwise
+// (Cin/G = 1) and grouped convolutions with at most 32 output channels per
+// group.
+//
+// The implicit-GEMM kernel tiles 64 output channels; a group with M = Cout/G
+// of 8 would leave seven eighths of every tile idle, and a depthwise layer
+// (K = KH*KW) has too little reuse to feed it. Here a block owns one group of
+// one image and a band of output rows. It copies the input rows the band
+// reads, for the group's channels, into shared memory with the zero border
+// written at copy time (the pages' padding at gather time), then each thread
+// computes all M output channels of a few pixels of the band from there,
+// with the group's weights broadcast from shared memory.
+//
+// Each output is still the pages' per-output loop: one accumulator from +0,
+// taps in (channel, kernel row, kernel column) order, the product formed at
+// every tap (an input position outside the plane contributes w * (+0)),
+// exact mode rounding the product and the sum separately, fast mode one
+// fused multiply-add (OneModel operators page, "Convolution"; the depthwise
+// workload of the convolution page).
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "om_device.cuh"
+#include "om_internal.h"
+
+namespace om {
+namespace {
+
+constexpr int kDirectThreads = 128;
+// Shared memory of one block: weights, tap table and input window.
+constexpr int64_t kDirectWindowBytes = 64 * 1024;
+
+struct DirectGeom {
+    const float *x;
+    const float *w;
+    float *y;
+    int H, W, HW, OH, OW, P;
+    int Cin, Cout, cin_g, M, K, w_ld;
+    int KH, KW, sH, sW, pT, pL, dH, dW;
+    int R;       // output rows per band
+    int WR, Wp;  // window rows (for R output rows) and columns
+    int wfloats, tints;  // weight floats and table ints, each a multiple of 4
+    Epilogue ep;
+};
+
+// Adds one tap's products w[oc] * v for the MB output channels of a pixel.
+template <int MODE, int MB>
+__device__ __forceinline__ void direct_tap(float2 (&acc)[(MB + 1) / 2], float &acc1,
+                                           const float *wt, float v) {
+    if constexpr (MB == 1) {
+        acc1 = term<MODE>(acc1, wt[0], v);
+    } else if constexpr (MB == 2) {
+        const float2 w2 = *reinterpret_cast<const float2 *>(wt);
+        acc[0] = term2<MODE>(acc[0], w2, make_float2(v, v));
+    } else {
+        const float2 v2 = make_float2(v, v);
+#pragma unroll
+        for (int q = 0; q < MB / 4; ++q) {
+            const float4 w4 = reinterpret_cast<const float4 *>(wt)[q];
+            acc[2 * q] = term2<MODE>(acc[2 * q], make_float2(w4.x, w4.y), v2);
+            acc[2 * q + 1] = term2<MODE>(acc[2 * q + 1], make_float2(w4.z, w4.w), v2);
+        }
+    }
+}
+
+// Grid: x over bands of R output rows, y over groups, z over images.
+// Shared memory: the group's weights tap-major (MB per tap, +0 for channels
+// past M); per tap its window offset c*WR*Wp + ky*dH*Wp + kx*dW; the window,
+// channel-major, WR rows of Wp columns, column j holding input column
+// j - pL (+0 outside the plane); then PX*sW floats of slack that only lanes
+// past the last output column read.
+// Thread pixels: unit (row r, q) covers columns q, q + QX, ... (QX =
+// ceil(OW/PX)), so neighbouring lanes read neighbouring window columns.
+template <int MODE, int MB, int PX>
+__global__ void __launch_bounds__(kDirectThreads) conv_direct_kernel(const DirectGeom g) {
+    extern __shared__ float4 smem4[];
+    float *wsm = reinterpret_cast<float *>(smem4);
+    int *tab = reinterpret_cast<int *>(wsm + g.wfloats);
+    float *win = reinterpret_cast<float *>(tab + g.tints);
+    const int grp = blockIdx.y;
+    const int64_t img = blockIdx.z;
+    const int oy0 = blockIdx.x * g.R;
+    const int rows = min(g.R, g.OH - oy0);
+    const int wr = (rows - 1) * g.sH + (g.KH - 1) * g.dH + 1;  // window rows this band reads
+    const int iy_base = oy0 * g.sH - g.pT;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+    // input window, zero border written here
+    const float *xg = g.x + (img * g.Cin + static_cast<int64_t>(grp) * g.cin_g) * g.HW;
+    const uint32_t win32 = smem_u32(win);
+    for (int c = 0; c < g.cin_g; ++c) {
+        const float *xc = xg + static_cast<int64_t>(c) * g.HW - g.pL;
+        for (int r = warp; r < wr; r += kDirectThreads / 32) {
+            const int iy = iy_base + r;
+            const bool row_ok = static_cast<unsigned>(iy) < static_cast<unsigned>(g.H);
+            const float *xrow = xc + static_cast<int64_t>(iy) * g.W;
+            const uint32_t drow = win32 + static_cast<uint32_t>((c * g.WR + r) * g.Wp) * 4u;
+            for (int j = lane; j < g.Wp; j += 32) {
+                const int ix = j - g.pL;
+                const bool ok = row_ok && static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
+                cp_async_4_if(drow + j * 4u, ok ? xrow + j : g.x, ok);
+            }
+        }
+    }
+    for (int i = tid; i < g.K * MB; i += kDirectThreads) {
+        const int t = i / MB, oc = i - (i / MB) * MB;
+        wsm[i] = oc < g.M ? g.w[static_cast<int64_t>(grp * g.M + oc) * g.w_ld + t] : 0.0f;
+    }
+    const int taps = g.KH * g.KW;
+    for (int t = tid; t < g.K; t += kDirectThreads) {
+        const int c = t / taps, rr = t - (t / taps) * taps;
+        const int ky = rr / g.KW, kx = rr - (rr / g.KW) * g.KW;
+        tab[t] = (c * g.WR + ky * g.dH) * g.Wp + kx * g.dW;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    const int qx = (g.OW + PX - 1) / PX;
+    for (int u = tid; u < rows * qx; u += kDirectThreads) {
+        const int ry = u / qx, q = u - (u / qx) * qx;
+        const float *wb = win + ry * g.sH * g.Wp + q * g.sW;
+        float2 acc[PX][(MB + 1) / 2];
+        float acc1[PX];
+#pragma unroll
+        for (int j = 0; j < PX; ++j) {
+            acc1[j] = 0.0f;
+#pragma unroll
+            for (int h = 0; h < (MB + 1) / 2; ++h) acc[j][h] = make_float2(0.0f, 0.0f);
+        }
+        const int step = qx * g.sW;  // window columns between the thread's pixels
+#pragma unroll 2
+        for (int t = 0; t < g.K; ++t) {
+            const float *src = wb + tab[t];
+            const float *wt = wsm + t * MB;
+#pragma unroll
+            for (int j = 0; j < PX; ++j) direct_tap<MODE, MB>(acc[j], acc1[j], wt, src[j * step]);
+        }
+        const int oy = oy0 + ry;
+        float *yp = g.y + (img * g.Cout + static_cast<int64_t>(grp) * g.M) * g.P +
+                    static_cast<int64_t>(oy) * g.OW + q;
+        const bool ep = g.ep.bias || g.ep.res || g.ep.act;
+#pragma unroll
+        for (int j = 0; j < PX; ++j) {
+            if (q + j * qx >= g.OW) break;
+#pragma unroll
+            for (int oc = 0; oc < MB; ++oc) {
+                if (oc < g.M) {
+                    float v = MB == 1 ? acc1[j] : ((oc & 1) ? acc[j][oc / 2].y : acc[j][oc / 2].x);
+                    float *o = yp + static_cast<int64_t>(oc) * g.P + j * qx;
+                    if (ep)
+                        v = epilogue_value(v, g.ep.bias ? g.ep.bias + grp * g.M + oc : nullptr,
+                                           g.ep.res ? g.ep.res + (o - g.y) : nullptr, g.ep.act);
+                    *o = canonical_nan(v);
+                }
+            }
+        }
+    }
+}
+
+template <int MODE, int MB, int PX>
+cudaError_t launch_direct(const DirectGeom &g, int64_t groups, int64_t images, size_t smem,
+                          cudaStream_t s) {
+    auto kernel = conv_direct_kernel<MODE, MB, PX>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>((g.OH + g.R - 1) / g.R), static_cast<unsigned>(groups),
+                    static_cast<unsigned>(images));
+    kernel<<<grid, kDirectThreads, smem, s>>>(g);
+    return cudaGetLastError();
+}
+
+// Pixels per thread PX (1, 2, 4 or 8): up to 32 accumulators (PX * MB) per thread.
+template <int MODE, int MB>
+cudaError_t launch_direct_px(const DirectGeom &g, int64_t groups, int64_t images, int px,
+                             size_t smem, cudaStream_t s) {
+    if constexpr (MB <= 4) {
+        if (px == 8) return launch_direct<MODE, MB, 8>(g, groups, images, smem, s);
+    }
+    if constexpr (MB <= 8) {
+        if (px == 4) return launch_direct<MODE, MB, 4>(g, groups, images, smem, s);
+    }
+    if constexpr (MB <= 16) {
+        if (px == 2) return launch_direct<MODE, MB, 2>(g, groups, images, smem, s);
+    }
+    return launch_direct<MODE, MB, 1>(g, groups, images, smem, s);
+}
+
+template <int MODE>
+cudaError_t launch_direct_mode(const DirectGeom &g, int64_t groups, int64_t images, int mb, int px,
+                               size_t smem, cudaStream_t s) {
+    switch (mb) {
+        case 1: return launch_direct_px<MODE, 1>(g, groups, images, px, smem, s);
+        case 2: return launch_direct_px<MODE, 2>(g, groups, images, px, smem, s);
+        case 4: return launch_direct_px<MODE, 4>(g, groups, images, px, smem, s);
+        case 8: return launch_direct_px<MODE, 8>(g, groups, images, px, smem, s);
+        case 16: return launch_direct_px<MODE, 16>(g, groups, images, px, smem, s);
+        case 32: return launch_direct_px<MODE, 32>(g, groups, images, px, smem, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace
+
+int conv_direct_channels(int64_t M) {
+    for (int mb = 1; mb <= kConvDirectMaxM; mb *= 2)
+        if (M <= mb) return mb;
+    return 0;
+}
+
+cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s) {
+    const int64_t M = p.Cout / p.G;
+    const int mb = conv_direct_channels(M);
+    if (mb == 0) return cudaErrorNotSupported;
+    if (p.N == 0 || p.OH * p.OW == 0) return cudaSuccess;
+    // all shared-memory offsets and per-image offsets in 32 bits
+    constexpr int64_t kCoordMax = int64_t{1} << 24;
+    if (p.H > kCoordMax || p.W > kCoordMax || p.pT > kCoordMax || p.pL > kCoordMax ||
+        p.sH > kCoordMax || p.sW > kCoordMax || p.dH * p.KH > kCoordMax ||
+        p.dW * p.KW > kCoordMax || p.G > 65535 || p.N > 65535 || p.w_ld > 0x7FFFFFFF ||
+        p.Cin * p.H * p.W > 0x7FFFFFFF || p.Cout * p.OH * p.OW > 0x7FFFFFFF)
+        return cudaErrorNotSupported;
+    // Pixels per thread: the most (up to 32 accumulators) that still leave
+    // about half of the GPU's thread slots busy.
+    const int64_t pixels = p.N * p.G * p.OH;
+    const int64_t busy = static_cast<int64_t>(num_sms()) * 1024;
+    int64_t px = 1;
+    for (int64_t c = 2; c <= 8 && c * mb <= 32; c *= 2)
+        if (pixels * ((p.OW + c - 1) / c) >= busy) px = c;
+    const int64_t cin_g = p.Cin / p.G;
+    const int64_t wp = (p.OW - 1) * p.sW + (p.KW - 1) * p.dW + 1;
+    const int64_t wfloats = (p.K * mb + 3) / 4 * 4, tints = (p.K + 3) / 4 * 4;
+    const int64_t fixed = (wfloats + tints + px * p.sW) * 4;
+    auto window_bytes = [&](int64_t R) {
+        return cin_g * ((R - 1) * p.sH + (p.KH - 1) * p.dH + 1) * wp * 4;
+    };
+    if (fixed + window_bytes(1) > kDirectWindowBytes) return cudaErrorNotSupported;
+    // the most output rows whose window fits, then fewer if that leaves
+    // fewer than two blocks per SM
+    int64_t R = p.OH;
+    while (R > 1 && fixed + window_bytes(R) > kDirectWindowBytes) R = (R + 1) / 2;
+    while (fixed + window_bytes(R + 1) <= kDirectWindowBytes && R < p.OH) ++R;
+    const int64_t want = 2 * static_cast<int64_t>(num_sms());
+    const int64_t planes = p.N * p.G;
+    if (planes * ((p.OH + R - 1) / R) < want) {
+        const int64_t bands = std::min<int64_t>(p.OH, (want + planes - 1) / planes);
+        R = std::max<int64_t>(1, (p.OH + bands - 1) / bands);
+    }
+    DirectGeom g;
+    g.x = p.x; g.w = p.w; g.y = p.y;
+    g.H = static_cast<int>(p.H); g.W = static_cast<int>(p.W); g.HW = static_cast<int>(p.H * p.W);
+    g.OH = static_cast<int>(p.OH); g.OW = static_cast<int>(p.OW); g.P = static_cast<int>(p.OH * p.OW);
+    g.Cin = static_cast<int>(p.Cin); g.Cout = static_cast<int>(p.Cout);
+    g.cin_g = static_cast<int>(cin_g); g.M = static_cast<int>(M);
+    g.K = static_cast<int>(p.K); g.w_ld = static_cast<int>(p.w_ld);
+    g.KH = static_cast<int>(p.KH); g.KW = static_cast<int>(p.KW);
+    g.sH = static_cast<int>(p.sH); g.sW = static_cast<int>(p.sW);
+    g.pT = static_cast<int>(p.pT); g.pL = static_cast<int>(p.pL);
+    g.dH = static_cast<int>(p.dH); g.dW = static_cast<int>(p.dW);
+    g.R = static_cast<int>(R);
+    g.WR = static_cast<int>((R - 1) * p.sH + (p.KH - 1) * p.dH + 1);
+    g.Wp = static_cast<int>(wp);
+    g.wfloats = static_cast<int>(wfloats); g.tints = static_cast<int>(tints);
+    g.ep = p.ep;
+    const size_t smem = static_cast<size_t>(fixed + window_bytes(R));
+    const int pxi = static_cast<int>(px);
+    return mode == kFast ? launch_direct_mode<kFast>(g, p.G, p.N, mb, pxi, smem, s)
+                         : launch_direct_mode<kExact>(g, p.G, p.N, mb, pxi, smem, s);
+}
+
+}  // namespace om

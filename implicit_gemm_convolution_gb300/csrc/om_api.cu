@@ -162,7 +162,11 @@ int pick_gemm_cfg(const GemmProblem &p, bool balanced) {
 int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     const int cfg = forced("OM_FORCE_CONV_CFG");
     if (cfg == om::kConvNaive || p.K == 0) return from_cuda(om::launch_conv_naive(p, mode, s));
-    cudaError_t e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
+    cudaError_t e = cudaErrorNotSupported;
+    if (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM))
+        e = om::launch_conv_direct(p, mode, s);
+    if (e == cudaErrorNotSupported && cfg != om::kConvDirect)
+        e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
     return from_cuda(e);
 }

@@ -62,7 +62,19 @@ enum ConvCfg : int {
     kConvAuto = -1,
     kConvNaive = 0,     // one thread per output, direct loops
     kConvImplicit = 1,  // implicit GEMM with gathered patches, 64 x 256 tiles
+    kConvDirect = 2,    // one thread per output pixel and group, all of its channels
 };
+
+// The direct kernel serves groups of up to kConvDirectMaxM output channels
+// whose weights, tap table and an input window of at least one output row
+// fit in its shared memory; the dispatcher takes it by itself up to
+// kConvDirectAutoM channels per group.
+constexpr int kConvDirectMaxM = 32;
+constexpr int kConvDirectAutoM = 16;
+// Channels the direct kernel computes per thread for M channels per group
+// (M rounded up to a power of two), or 0 above kConvDirectMaxM.
+int conv_direct_channels(int64_t M);
+cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s);
 
 cudaError_t launch_gemm_naive(const GemmProblem &p, int mode, cudaStream_t s);
 cudaError_t launch_conv_naive(const ConvProblem &p, int mode, cudaStream_t s);

@@ -11,7 +11,7 @@ from tests.gpu_util import (assert_bits_equal, forced_config, guarded_output, gu
 pytestmark = pytest.mark.gpu
 
 MODES = [(oracle.EXACT, "exact"), (oracle.FAST, "fast")]
-CFGS = [0, None]  # direct kernel, default dispatch
+CFGS = [0, 1, 2, None]  # naive, implicit GEMM, direct small-group kernel, default dispatch
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -80,6 +80,12 @@ SMALL = [
     # K = 9216 taps: the tap table would not fit in shared memory beside the
     # stages, so the per-element gather runs
     (1, 1024, 6, 5, 8, 1, 3, 3, 1, 1, 1),
+    # depthwise and small groups (the direct kernel's shapes): multiplier 1,
+    # 2 and 3, a 5x5 dilated kernel, 32 channels per group
+    (2, 32, 15, 15, 32, 32, 3, 3, 1, 1, 1),
+    (1, 16, 20, 20, 32, 16, 3, 3, 2, 1, 1),
+    (2, 24, 9, 9, 72, 24, 5, 5, 1, 2, 2),
+    (2, 64, 10, 10, 64, 2, 3, 3, 1, 1, 1),
 ]
 
 
@@ -189,3 +195,20 @@ def test_1x1_input_not_16_byte_aligned(mode, name):
     assert st == 0
     torch.cuda.synchronize()
     assert_bits_equal(y.cpu().numpy(), want_conv(c, mode), "misaligned 1x1")
+
+
+# Shapes with enough output pixels that the direct small-group kernel gives
+# each thread 4 (depthwise; 8 channels per group) or 2 (4 channels) pixels.
+DIRECT_WIDE = [
+    (4, 64, 56, 56, 64, 64, 3, 3, 1, 1, 1),
+    (4, 128, 48, 48, 256, 64, 3, 3, 1, 1, 1),
+    (8, 64, 56, 56, 256, 32, 3, 3, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("shape", DIRECT_WIDE)
+@pytest.mark.parametrize("mode,name", MODES)
+def test_direct_kernel_several_pixels_per_thread(shape, mode, name):
+    c = synth.make_conv("t", *shape, seed=sum(shape) + 5, dist_x=("uniform", -1, 1),
+                        dist_w=("normal", 0, 0.5))
+    assert_bits_equal(run_conv(c, name), want_conv(c, mode), f"direct {shape}")
