@@ -1,0 +1,402 @@
+// Matrix-vector products: a product with at most 8 rows (C = a . B, the
+// decode-shaped GEMM) or at most 8 columns (C = A . b, which is also a 1x1
+// convolution over a 1x1 input: a fully connected layer over a few images).
+//
+// Both are bound by streaming the large operand from HBM once. The tiled
+// kernels would leave most of a 128-row (or 256-column) tile idle, so here a
+// block owns a strip of 32 output columns (or rows): one producer warp
+// streams the large operand's strip through a ring of shared-memory stages
+// with TMA (cp.async when its rows are not 16-byte aligned) behind mbarrier
+// full/empty pairs, and each of 32 consumer threads keeps all the few outputs
+// of its own column (or row) in registers. Every output is still one
+// sequential loop over k from +0, exact mode rounding product and sum
+// separately, fast mode one fused multiply-add per term; rows past k are
+// zero-filled on both operands, which adds +0 * +0 = +0 to an accumulator
+// that is never -0 (OneModel operators page, "Matrix product"; the
+// matrix-vector product page).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "om_device.cuh"
+#include "om_internal.h"
+
+namespace om {
+
+__device__ unsigned g_status_gemv;
+
+namespace {
+
+constexpr int kGemvOut = 32;      // outputs (columns or rows) per block, one per consumer thread
+constexpr int kGemvRS = 32;       // k per stage
+constexpr int kGemvStages = 12;   // ring depth
+constexpr int kGemvThreads = kGemvOut + 32;  // consumers, then one producer warp
+constexpr int kGemvConsumerWarps = kGemvOut / 32;
+constexpr uint32_t kBigBytes = kGemvOut * kGemvRS * 4;  // large-operand tile of a stage
+
+// Shared memory: the large operand's stages (1 KB aligned, as the 128-byte
+// swizzle wants), the small operand's stages, then the full and empty
+// barriers of the ring.
+template <int R>
+struct GemvSmem {
+    static constexpr uint32_t kSmallBytes = kGemvRS * R * 4;
+    static constexpr uint32_t kSmallOff = kGemvStages * kBigBytes;
+    static constexpr uint32_t kBarOff = kSmallOff + kGemvStages * kSmallBytes;
+    static constexpr uint32_t kBytes = 1024 + kBarOff + 2 * kGemvStages * 8;
+};
+
+// Strided operands: X(r, c) = X[r * sr + c * sc].
+struct GemvProblem {
+    int64_t m, n, k;
+    const float *A;  // A(i, p)
+    int64_t a_si, a_sp;
+    const float *B;  // B(p, j)
+    int64_t b_sp, b_sj;
+    float *C;  // C(i, j)
+    int64_t c_si, c_sj;
+    const float *bias;  // bias(i, j) = bias[i * bias_si + j * bias_sj]
+    int64_t bias_si, bias_sj;
+    const float *res;  // res(i, j) = res[i * res_si + j * res_sj]
+    int64_t res_si, res_sj;
+    int act;
+    // per blockIdx.y (group) offsets of A rows, B rows, C rows, bias and res,
+    // and the row of the group's first A row in A's tensor map
+    int64_t grp_a, grp_b, grp_c, grp_bias, grp_res;
+    int64_t grp_map_rows;
+};
+
+__device__ __forceinline__ float gemv_epilogue(const GemvProblem &g, float v, int64_t i, int64_t j,
+                                               int grp) {
+    if (g.bias || g.res || g.act)
+        v = epilogue_value(v, g.bias ? g.bias + grp * g.grp_bias + i * g.bias_si + j * g.bias_sj : nullptr,
+                           g.res ? g.res + grp * g.grp_res + i * g.res_si + j * g.res_sj : nullptr, g.act);
+    return canonical_nan(v);
+}
+
+__device__ __forceinline__ uint8_t *gemv_smem_base(uint8_t *raw) {
+    const uint32_t b = smem_u32(raw);
+    return raw + ((1024u - (b & 1023u)) & 1023u);
+}
+
+__device__ __forceinline__ void gemv_record_timeout() { atomicOr(&g_status_gemv, kDevErrTimeout); }
+
+// Producer warp of both kernels. Stage kt: the large operand's tile by TMA
+// (lane 0, when TMA) or by 4-byte copies of every lane, and the small
+// operand's tile by 4-byte copies; each lane's copies arrive on the stage's
+// full barrier as they land.
+template <int R, bool ROWS, bool TMA>
+__device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtensorMap *map,
+                                             uint8_t *base, uint64_t *full, uint64_t *empty,
+                                             int nk, int lane) {
+    using Sm = GemvSmem<R>;
+    const int grp = blockIdx.y;
+    const int64_t o0 = static_cast<int64_t>(blockIdx.x) * kGemvOut;  // first output column / row
+    const float *A = g.A + grp * g.grp_a;
+    const float *B = g.B + grp * g.grp_b;
+    const uint32_t base32 = smem_u32(base);
+    for (int kt = 0; kt < nk; ++kt) {
+        const int s = kt % kGemvStages;
+        if (!mbar_wait(&empty[s], ((kt / kGemvStages) & 1) ^ 1)) {
+            gemv_record_timeout();
+            cp_async_wait_all();
+            if (TMA && lane == 0) {
+                // let the tiles already requested land before leaving
+                for (int s2 = 0; s2 < kGemvStages && s2 < kt; ++s2) {
+                    const int last = s2 + ((kt - 1 - s2) / kGemvStages) * kGemvStages;
+                    (void)mbar_wait(&full[s2], static_cast<uint32_t>((last / kGemvStages) & 1));
+                }
+            }
+            return;
+        }
+        const int64_t p0 = static_cast<int64_t>(kt) * kGemvRS;
+        uint8_t *big = base + s * kBigBytes;
+        const uint32_t big32 = base32 + s * kBigBytes;
+        const uint32_t small32 = base32 + Sm::kSmallOff + s * Sm::kSmallBytes;
+        if constexpr (TMA) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], kBigBytes);
+                if constexpr (ROWS)
+                    tma_load_2d(big, map, &full[s], static_cast<int>(o0), static_cast<int>(p0));
+                else
+                    tma_load_2d(big, map, &full[s], static_cast<int>(p0),
+                                static_cast<int>(grp * g.grp_map_rows + o0));
+            }
+        } else if constexpr (ROWS) {
+            // B rows of the stage, [32][32]
+            for (int e = lane; e < kGemvRS * kGemvOut; e += 32) {
+                const int r = e / kGemvOut, c = e % kGemvOut;
+                const int64_t p = p0 + r, j = o0 + c;
+                const bool ok = p < g.k && j < g.n;
+                cp_async_4_if(big32 + e * 4, ok ? B + p * g.b_sp + j * g.b_sj : B, ok);
+            }
+        } else {
+            // A rows of the block, [32][32], 16-byte chunk c of row r at c ^ (r % 8)
+            for (int e = lane; e < kGemvOut * kGemvRS; e += 32) {
+                const int r = e / kGemvRS, kk = e % kGemvRS;
+                const int64_t i = o0 + r, p = p0 + kk;
+                const bool ok = i < g.m && p < g.k;
+                const uint32_t off = (r * kGemvRS + ((((kk >> 2) ^ (r & 7)) << 2) | (kk & 3))) * 4;
+                cp_async_4_if(big32 + off, ok ? A + i * g.a_si + p * g.a_sp : A, ok);
+            }
+        }
+        // the small operand: A columns [32][R] (few rows) or B rows [32][R] (few columns)
+        for (int e = lane; e < kGemvRS * R; e += 32) {
+            const int r = e / R, q = e % R;
+            const int64_t p = p0 + r;
+            bool ok;
+            const float *src;
+            if constexpr (ROWS) {
+                ok = p < g.k && q < g.m;
+                src = ok ? A + q * g.a_si + p * g.a_sp : A;
+            } else {
+                ok = p < g.k && q < g.n;
+                src = ok ? B + p * g.b_sp + q * g.b_sj : B;
+            }
+            cp_async_4_if(small32 + e * 4, src, ok);
+        }
+        cp_async_arrive_noinc(&full[s]);
+    }
+    cp_async_wait_all();
+}
+
+// C (m x n) = A (m x k) . B (k x n) with m <= R (ROWS: a block owns 32
+// columns) or n <= R (!ROWS: a block owns 32 rows of group blockIdx.y).
+// TMA: the large operand comes by a 2-D tensor map (ROWS: B, box 32 columns
+// x 32 rows; !ROWS: A, box 32 k x 32 rows with the 128-byte swizzle).
+template <int MODE, int R, bool ROWS, bool TMA>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap map, const GemvProblem g) {
+    using Sm = GemvSmem<R>;
+    extern __shared__ uint8_t gemv_raw[];
+    uint8_t *base = gemv_smem_base(gemv_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + Sm::kBarOff);
+    uint64_t *empty = full + kGemvStages;
+    const int nk = static_cast<int>((g.k + kGemvRS - 1) / kGemvRS);
+    const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+    if (t == 0) {
+        for (int s = 0; s < kGemvStages; ++s) {
+            mbar_init(&full[s], 32 + (TMA ? 1 : 0));
+            mbar_init(&empty[s], kGemvConsumerWarps);
+        }
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (warp == kGemvConsumerWarps) {
+        if (TMA && lane == 0) prefetch_tensormap(&map);
+        gemv_produce<R, ROWS, TMA>(g, &map, base, full, empty, nk, lane);
+        return;
+    }
+
+    float2 acc[(R + 1) / 2];
+    float acc1 = 0.0f;
+#pragma unroll
+    for (int h = 0; h < (R + 1) / 2; ++h) acc[h] = make_float2(0.0f, 0.0f);
+#pragma unroll 1
+    for (int kt = 0; kt < nk; ++kt) {
+        const int s = kt % kGemvStages;
+        if (!mbar_wait(&full[s], (kt / kGemvStages) & 1)) {
+            gemv_record_timeout();
+            return;
+        }
+        const float *big = reinterpret_cast<const float *>(base + s * kBigBytes);
+        const float *small = reinterpret_cast<const float *>(base + Sm::kSmallOff + s * Sm::kSmallBytes);
+        if constexpr (ROWS) {
+            const float *bcol = big + t;
+#pragma unroll
+            for (int r = 0; r < kGemvRS; ++r) {
+                const float b = bcol[r * kGemvOut];
+                if constexpr (R == 1) {
+                    acc1 = term<MODE>(acc1, small[r], b);
+                } else {
+                    const float2 b2 = make_float2(b, b);
+#pragma unroll
+                    for (int h = 0; h < R / 2; ++h)
+                        acc[h] = term2<MODE>(acc[h], reinterpret_cast<const float2 *>(small + r * R)[h], b2);
+                }
+            }
+        } else {
+            const float4 *arow = reinterpret_cast<const float4 *>(big + t * kGemvRS);
+#pragma unroll
+            for (int c = 0; c < kGemvRS / 4; ++c) {
+                const float4 a4 = arow[c ^ (t & 7)];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float a = q == 0 ? a4.x : q == 1 ? a4.y : q == 2 ? a4.z : a4.w;
+                    const float *brow = small + (4 * c + q) * R;
+                    if constexpr (R == 1) {
+                        acc1 = term<MODE>(acc1, a, brow[0]);
+                    } else {
+                        const float2 a2 = make_float2(a, a);
+#pragma unroll
+                        for (int h = 0; h < R / 2; ++h)
+                            acc[h] = term2<MODE>(acc[h], a2, reinterpret_cast<const float2 *>(brow)[h]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    const int grp = blockIdx.y;
+    const int64_t o = static_cast<int64_t>(blockIdx.x) * kGemvOut + t;
+    if (o >= (ROWS ? g.n : g.m)) return;
+    float *C = g.C + grp * g.grp_c;
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+        if (q < (ROWS ? g.m : g.n)) {
+            const float v = R == 1 ? acc1 : ((q & 1) ? acc[q / 2].y : acc[q / 2].x);
+            const int64_t i = ROWS ? q : o, j = ROWS ? o : q;
+            C[i * g.c_si + j * g.c_sj] = gemv_epilogue(g, v, i, j, grp);
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 gemv_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Row-major matrix (rows x cols, row stride ld floats) with box
+// box_cols x box_rows; +0 outside. False when TMA cannot describe it.
+bool gemv_map(CUtensorMap *map, const float *base, int64_t rows, int64_t cols, int64_t ld,
+              int box_cols, int box_rows, bool swizzle128) {
+    auto fn = gemv_encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || ld % 4 != 0 || rows < 1 || cols < 1 ||
+        rows > (int64_t{1} << 31) || cols > (int64_t{1} << 31))
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int round_up_pow2(int64_t v) {
+    int r = 1;
+    while (r < v) r *= 2;
+    return r;
+}
+
+template <int MODE, int R, bool ROWS, bool TMA>
+cudaError_t launch_one(const CUtensorMap &map, const GemvProblem &g, int64_t blocks, int64_t groups,
+                       cudaStream_t s) {
+    auto kernel = gemv_kernel<MODE, R, ROWS, TMA>;
+    const int smem = static_cast<int>(GemvSmem<R>::kBytes);
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(groups)), kGemvThreads, smem, s>>>(map, g);
+    return cudaGetLastError();
+}
+
+template <int MODE, bool ROWS, bool TMA>
+cudaError_t launch_r(const CUtensorMap &map, const GemvProblem &g, int r, int64_t blocks, int64_t groups,
+                     cudaStream_t s) {
+    switch (r) {
+        case 1: return launch_one<MODE, 1, ROWS, TMA>(map, g, blocks, groups, s);
+        case 2: return launch_one<MODE, 2, ROWS, TMA>(map, g, blocks, groups, s);
+        case 4: return launch_one<MODE, 4, ROWS, TMA>(map, g, blocks, groups, s);
+        case 8: return launch_one<MODE, 8, ROWS, TMA>(map, g, blocks, groups, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap &map, const GemvProblem &g, bool rows, bool tma, int r,
+                        int64_t blocks, int64_t groups, cudaStream_t s) {
+    if (rows)
+        return tma ? launch_r<MODE, true, true>(map, g, r, blocks, groups, s)
+                   : launch_r<MODE, true, false>(map, g, r, blocks, groups, s);
+    return tma ? launch_r<MODE, false, true>(map, g, r, blocks, groups, s)
+               : launch_r<MODE, false, false>(map, g, r, blocks, groups, s);
+}
+
+// map_rows: rows of the large operand's tensor map (!rows: all groups' A
+// rows); the map is built here when the operand allows it.
+cudaError_t launch_gemv(const GemvProblem &g, int mode, bool rows, int64_t groups, int64_t map_rows,
+                        int64_t map_ld, cudaStream_t s) {
+    const int64_t small = rows ? g.m : g.n;
+    const int64_t big = rows ? g.n : g.m;
+    if (small < 1 || small > kGemvMaxSmall || g.k < 1 || groups < 1 || groups > 65535 ||
+        g.k > 0x7FFFFFFF - kGemvRS)
+        return cudaErrorNotSupported;
+    const int64_t blocks = (big + kGemvOut - 1) / kGemvOut;
+    if (blocks > 0x7FFFFFFF) return cudaErrorNotSupported;
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    bool tma;
+    if (rows)
+        tma = g.b_sj == 1 && gemv_map(&map, g.B, g.k, g.n, g.b_sp, kGemvOut, kGemvRS, false);
+    else
+        tma = g.a_sp == 1 && map_rows <= 0x7FFFFFFF - kGemvOut &&
+              gemv_map(&map, g.A, map_rows, g.k, map_ld, kGemvRS, kGemvOut, true);
+    const int r = round_up_pow2(small);
+    return mode == kFast ? launch_mode<kFast>(map, g, rows, tma, r, blocks, groups, s)
+                         : launch_mode<kExact>(map, g, rows, tma, r, blocks, groups, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_gemv(const GemmProblem &p, int mode, cudaStream_t s) {
+    GemvProblem g{};
+    g.m = p.m; g.n = p.n; g.k = p.k;
+    g.A = p.A; g.a_si = p.lda; g.a_sp = 1;
+    g.B = p.B; g.b_sp = p.ldb; g.b_sj = 1;
+    g.C = p.C; g.c_si = p.ldc; g.c_sj = 1;
+    g.bias = p.ep.bias; g.bias_si = 0; g.bias_sj = 1;
+    g.res = p.ep.res; g.res_si = p.ep.ldr; g.res_sj = 1;
+    g.act = p.ep.act;
+    if (p.m <= kGemvMaxSmall) return launch_gemv(g, mode, true, 1, 0, 0, s);
+    if (p.n <= kGemvMaxSmall) return launch_gemv(g, mode, false, 1, p.m, p.lda, s);
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s) {
+    // a 1x1 kernel over a 1x1 input with no padding: per group, output
+    // channel oc of image n is the product of weight row oc with the image's
+    // input channels
+    if (p.KH != 1 || p.KW != 1 || p.H != 1 || p.W != 1 || p.pT != 0 || p.pL != 0 || p.OH != 1 ||
+        p.OW != 1 || p.N > kGemvMaxSmall || p.N < 1)
+        return cudaErrorNotSupported;
+    const int64_t M = p.Cout / p.G, cin_g = p.Cin / p.G;
+    GemvProblem g{};
+    g.m = M; g.n = p.N; g.k = cin_g;
+    g.A = p.w; g.a_si = p.w_ld; g.a_sp = 1;
+    g.B = p.x; g.b_sp = 1; g.b_sj = p.Cin;
+    g.C = p.y; g.c_si = 1; g.c_sj = p.Cout;
+    g.bias = p.ep.bias; g.bias_si = 1; g.bias_sj = 0;
+    g.res = p.ep.res; g.res_si = 1; g.res_sj = p.Cout;
+    g.act = p.ep.act;
+    g.grp_a = M * p.w_ld; g.grp_b = cin_g; g.grp_c = M; g.grp_bias = M; g.grp_res = M;
+    g.grp_map_rows = M;
+    return launch_gemv(g, mode, false, p.G, p.Cout, p.w_ld, s);
+}
+
+cudaError_t read_clear_status_gemv(unsigned *out, cudaStream_t s) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status_gemv, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (*out) e = cudaMemcpyToSymbol(g_status_gemv, &zero, sizeof(unsigned));
+    return e;
+}
+
+}  // namespace om

@@ -163,9 +163,11 @@ int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     const int cfg = forced("OM_FORCE_CONV_CFG");
     if (cfg == om::kConvNaive || p.K == 0) return from_cuda(om::launch_conv_naive(p, mode, s));
     cudaError_t e = cudaErrorNotSupported;
-    if (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM))
+    if (cfg == om::kConvGemv || cfg < 0) e = om::launch_conv_gemv(p, mode, s);
+    if (e == cudaErrorNotSupported &&
+        (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM)))
         e = om::launch_conv_direct(p, mode, s);
-    if (e == cudaErrorNotSupported && cfg != om::kConvDirect)
+    if (e == cudaErrorNotSupported && cfg != om::kConvDirect && cfg != om::kConvGemv)
         e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
     return from_cuda(e);
@@ -234,6 +236,11 @@ int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, cons
     }
     int cfg = forced("OM_FORCE_GEMM_CFG");
     if (k == 0 || cfg == om::kCfgNaive) return from_cuda(om::launch_gemm_naive(p, mode, s));
+    if (cfg == om::kCfgGemv || (cfg < 0 && (m <= om::kGemvMaxSmall || n <= om::kGemvMaxSmall))) {
+        const cudaError_t eg = om::launch_gemm_gemv(p, mode, s);
+        if (eg != cudaErrorNotSupported) return from_cuda(eg);
+        cfg = -1;
+    }
     if (cfg < 0) cfg = pick_gemm_cfg(p, flags != nullptr);
     cudaError_t e = om::launch_gemm_tiled(p, mode, cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, mode, om::kCfgAsync128x128, flags, s);
@@ -409,11 +416,12 @@ int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout,
 
 int om_device_status(void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0;
     if (om::read_clear_status_gemm(&a, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_conv(&b, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_tc(&c, s) != cudaSuccess) return OM_ERR_CUDA;
-    return ((a | b | c) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
+    if (om::read_clear_status_gemv(&d, s) != cudaSuccess) return OM_ERR_CUDA;
+    return ((a | b | c | d) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
 }
 
 }  // extern "C"

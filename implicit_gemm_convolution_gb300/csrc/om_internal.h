@@ -56,13 +56,20 @@ enum GemmCfg : int {
     kCfgTma128x128 = 2,        // TMA-fed SIMT tiles, 128x128, paired-lane fp32
     kCfgAsync128x128 = 3,      // 4-byte cp.async-fed SIMT tiles (any alignment)
     kCfgTmaScalar128x256 = 4,  // as 1 with one-lane fp32 instructions
+    kCfgGemv = 5,              // matrix-vector kernel (at most 8 rows or 8 columns)
 };
+
+// The matrix-vector kernels take products with at most kGemvMaxSmall rows
+// or columns (and 1x1 convolutions over 1x1 inputs of at most that many
+// images).
+constexpr int kGemvMaxSmall = 8;
 
 enum ConvCfg : int {
     kConvAuto = -1,
     kConvNaive = 0,     // one thread per output, direct loops
     kConvImplicit = 1,  // implicit GEMM with gathered patches, 64 x 256 tiles
     kConvDirect = 2,    // one thread per output pixel and group, all of its channels
+    kConvGemv = 3,      // 1x1 over a 1x1 input: matrix-vector kernel
 };
 
 // The direct kernel serves groups of up to kConvDirectMaxM output channels
@@ -75,6 +82,11 @@ constexpr int kConvDirectAutoM = 16;
 // (M rounded up to a power of two), or 0 above kConvDirectMaxM.
 int conv_direct_channels(int64_t M);
 cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s);
+
+// Matrix-vector kernels; cudaErrorNotSupported when the shape is not theirs.
+cudaError_t launch_gemm_gemv(const GemmProblem &p, int mode, cudaStream_t s);
+cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s);
+cudaError_t read_clear_status_gemv(unsigned *out, cudaStream_t s);
 
 cudaError_t launch_gemm_naive(const GemmProblem &p, int mode, cudaStream_t s);
 cudaError_t launch_conv_naive(const ConvProblem &p, int mode, cudaStream_t s);
