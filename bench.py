@@ -309,7 +309,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     wsp = om.new_workspace(dev)
 
-    def gemm_line(name, mode, case_, use_ws=False):
+    def gemm_line(name, mode, case_, use_ws=False, hbm_bound=False):
         Ad = torch.from_numpy(case_.A).to(dev)
         Bd = torch.from_numpy(case_.B).to(dev)
         Cd = torch.from_numpy(case_.C_init).to(dev)
@@ -326,6 +326,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
         extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
                         "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
+        if hbm_bound:
+            extras[name].update(hbm_fields(4.0 * (case_.m * case_.k + case_.k * case_.n +
+                                                  case_.m * case_.n), t))
+
+    def hbm_fields(nbytes, t_ms):
+        """Algorithmic bytes (each operand read once, the output written once)
+        against the measured copy bandwidth, for HBM-bound kernels."""
+        gbs = nbytes / (t_ms * 1e-3) / 1e9
+        hbm = measured_peaks()["hbm_gbs"]
+        return {"bound": "hbm", "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+                "hbm_peak_gbs": hbm, "algorithmic_bytes": int(nbytes)}
 
     def tf32x3_line(name, case_):
         Ad = torch.from_numpy(case_.A).to(dev)
@@ -349,7 +360,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "tensor_peak_basis": peaks["basis"] + " x nominal tf32/bf16 ratio 1.1/2.25; "
                                              "three tensor-core products per useful flop"}
 
-    def conv_line(name, mode, c, use_ws=False):
+    def conv_line(name, mode, c, use_ws=False, hbm_bound=False):
         x = torch.from_numpy(c.x).to(dev)
         w = torch.from_numpy(c.w).to(dev)
         OH = om.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.dil)
@@ -373,6 +384,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
         extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
                         "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
+        if hbm_bound:
+            extras[name].update(hbm_fields(4.0 * (c.x.size + c.w.size + c.N * c.Cout * OH * OW), t))
 
     if not args.headline_only:
         gemm_line("gemm_4096^3_fast_ws", "fast", case, use_ws=True)
@@ -394,6 +407,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             conv_line(f"conv3x3_n32_c64_56_{md}", md, synth.workload_conv3x3())
             conv_line(f"conv1x1_n32_c256to64_56_{md}", md, synth.workload_conv1x1())
         conv_line("conv_g32_s2_d2_n16_c256_28_exact", "exact", synth.workload_conv_grouped())
+        conv_line("conv_g32_s2_d2_n16_c256_28_fast", "fast", synth.workload_conv_grouped())
+        for md in ("exact", "fast"):
+            conv_line(f"conv_dw3x3_n32_c256_56_{md}", md, synth.workload_conv_depthwise(),
+                      hbm_bound=True)
+            gemm_line(f"gemm_decode_1x11008x4096_{md}", md, synth.workload_gemm_decode(),
+                      hbm_bound=True)
 
     cpu = cpu_baseline(args.cpu_seconds)
     line = {
@@ -499,9 +518,11 @@ def run_profile(args):
     name, mode = args.profile.split(":")[:2]
     gemms = {"gemm_4096^3": synth.workload_gemm_4096,
              "gemm_prefill": lambda: synth.workload_gemm_prefill(False),
-             "gemm_prefill_ragged": lambda: synth.workload_gemm_prefill(True)}
+             "gemm_prefill_ragged": lambda: synth.workload_gemm_prefill(True),
+             "gemm_decode": synth.workload_gemm_decode}
     convs = {"conv3x3": synth.workload_conv3x3, "conv1x1": synth.workload_conv1x1,
-             "conv_grouped": synth.workload_conv_grouped}
+             "conv_grouped": synth.workload_conv_grouped,
+             "conv_depthwise": synth.workload_conv_depthwise}
     if name in gemms:
         case = gemms[name]()
         A = torch.from_numpy(case.A).to(dev)
@@ -546,8 +567,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--profile", default=None,
-                    help="workload:mode (gemm_4096^3, gemm_prefill, gemm_prefill_ragged, conv3x3,"
-                         " conv1x1, conv_grouped) -- launch only that kernel, for ncu")
+                    help="workload:mode (gemm_4096^3, gemm_prefill, gemm_prefill_ragged, gemm_decode,"
+                         " conv3x3, conv1x1, conv_grouped, conv_depthwise) -- launch only that"
+                         " kernel, for ncu")
     args = ap.parse_args()
     if args.profile:
         run_profile(args)

@@ -262,3 +262,15 @@ def workload_conv_grouped() -> ConvCase:
     return make_conv("conv_g32_s2_d2_n16_c256_28", 16, 256, 28, 28, 256, 32, 3, 3, 2, 1, 2, seed=6,
                      dist_x=("uniform", -1.0, 1.0), dist_w=("normal", 0.0, 0.1),
                      nonfinite_weights=18)
+
+
+# Widened workloads (not among the five above): a depthwise layer of
+# MobileNet-like shape and a one-token product with the prefill weights.
+def workload_conv_depthwise() -> ConvCase:
+    return make_conv("conv_dw3x3_n32_c256_56", 32, 256, 56, 56, 256, 256, 3, 3, 1, 1, 1, seed=7,
+                     dist_x=("uniform", 0.0, 1.0), dist_w=("normal", 0.0, math.sqrt(2.0 / 9)))
+
+
+def workload_gemm_decode() -> GemmCase:
+    return make_gemm("gemm_decode_1x11008x4096", 1, 11008, 4096, seed=8,
+                     dist_a=("normal", 0.0, 1.0), dist_b=("normal", 0.0, 0.02))
