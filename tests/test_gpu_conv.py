@@ -86,6 +86,16 @@ SMALL = [
     (1, 16, 20, 20, 32, 16, 3, 3, 2, 1, 1),
     (2, 24, 9, 9, 72, 24, 5, 5, 1, 2, 2),
     (2, 64, 10, 10, 64, 2, 3, 3, 1, 1, 1),
+    # depthwise 3x3 / 5x5 with stride 1 and 2 (the register-run kernel): ragged
+    # rows of 8 outputs, paddings 0-2, several row bands in one plane
+    (3, 16, 17, 23, 16, 16, 3, 3, 2, 1, 1),
+    (2, 24, 19, 13, 24, 24, 5, 5, 1, 2, 1),
+    (2, 12, 21, 30, 12, 12, 5, 5, 2, 2, 1),
+    (1, 8, 7, 7, 8, 8, 3, 3, 1, 0, 1),
+    (1, 4, 300, 260, 4, 4, 3, 3, 1, 1, 1),
+    # rows a multiple of 4 floats (16-byte window copies and stores)
+    (2, 8, 20, 32, 8, 8, 5, 5, 2, 2, 1),
+    (2, 8, 30, 64, 8, 8, 3, 3, 2, 1, 1),
 ]
 
 

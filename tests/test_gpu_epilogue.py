@@ -60,6 +60,8 @@ CONVS = [
     (2, 16, 12, 12, 64, 1, 3, 3, 1, 1, 1),
     (4, 32, 9, 11, 96, 2, 1, 1, 1, 0, 1),
     (3, 24, 6, 10, 40, 2, 1, 1, 1, 0, 1),
+    (2, 16, 14, 14, 16, 16, 3, 3, 1, 1, 1),
+    (2, 16, 12, 16, 16, 16, 3, 3, 1, 1, 1),
     (1, 8, 13, 13, 8, 8, 3, 3, 2, 1, 2),
 ]
 
