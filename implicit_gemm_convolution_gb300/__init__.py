@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
             L.om_pack_conv_weights.argtypes = [i64] * 5 + [vp, vp, ctypes.POINTER(ctypes.c_size_t), vp]
             L.om_device_status.restype = ci
             L.om_device_status.argtypes = [vp]
+            L.om_selftest_wait_timeout.argtypes = [ci, ci, vp]
             L.om_workspace_bytes.restype = ctypes.c_size_t
             L.om_gemm_f32_ex.restype = ci
             L.om_gemm_f32_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp, i64, ci,

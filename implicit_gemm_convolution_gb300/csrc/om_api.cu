@@ -416,12 +416,18 @@ int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout,
 
 int om_device_status(void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned a = 0, b = 0, c = 0, d = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0, e = 0;
     if (om::read_clear_status_gemm(&a, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_conv(&b, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_tc(&c, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_gemv(&d, s) != cudaSuccess) return OM_ERR_CUDA;
-    return ((a | b | c | d) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
+    if (om::read_clear_status_selftest(&e, s) != cudaSuccess) return OM_ERR_CUDA;
+    return ((a | b | c | d | e) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
+}
+
+int om_selftest_wait_timeout(int which, int limit_ms, void *stream) {
+    if ((which != 0 && which != 1) || limit_ms < 1 || limit_ms > 1000) return OM_ERR_INVALID_ARG;
+    return from_cuda(om::launch_wait_timeout(which, limit_ms, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

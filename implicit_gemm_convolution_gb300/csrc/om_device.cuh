@@ -147,15 +147,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after the
-// time limit (the caller records the error and leaves).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after
+// limit_ns (the caller records the error and leaves).
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity,
+                                                unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_limit(bar, parity, kWaitLimitNs);
+}
+
+// Wait until the global flag *f is non-zero, with acquire ordering; false
+// after limit_ns.
+__device__ __forceinline__ bool acquire_flag(const unsigned *f, unsigned long long limit_ns) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v != 0) return true;
+    const unsigned long long t0 = global_ns();
+    do {
+        __nanosleep(200);
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    } while (v == 0 && global_ns() - t0 <= limit_ns);
+    return v != 0;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -88,6 +88,11 @@ cudaError_t launch_gemm_gemv(const GemmProblem &p, int mode, cudaStream_t s);
 cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s);
 cudaError_t read_clear_status_gemv(unsigned *out, cudaStream_t s);
 
+// Failure-detection self-test (selftest.cu): a one-block kernel whose
+// bounded wait (0: mbarrier phase, 1: global flag) runs out after limit_ms.
+cudaError_t launch_wait_timeout(int which, int limit_ms, cudaStream_t s);
+cudaError_t read_clear_status_selftest(unsigned *out, cudaStream_t s);
+
 cudaError_t launch_gemm_naive(const GemmProblem &p, int mode, cudaStream_t s);
 cudaError_t launch_conv_naive(const ConvProblem &p, int mode, cudaStream_t s);
 cudaError_t launch_pack_conv_weights(int64_t Cout, int64_t K, int64_t Kp, const float *w,

@@ -265,17 +265,8 @@ __device__ __forceinline__ void signal_early_part(unsigned *flags, int consumers
 // Wait (bounded) for the previous CTA's early part; false on timeout.
 __device__ __forceinline__ bool wait_previous_part(unsigned *flags, int consumers, int *abort_flag) {
     if (threadIdx.x == 0) {
-        const unsigned *f = flags + blockIdx.x - 1;
-        unsigned v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-        if (v == 0) {
-            const unsigned long long t0 = global_ns();
-            do {
-                __nanosleep(200);
-                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-            } while (v == 0 && global_ns() - t0 <= kWaitLimitNs);
-        }
-        if (v == 0) *reinterpret_cast<volatile int *>(abort_flag) = 2;
+        if (!acquire_flag(flags + blockIdx.x - 1, kWaitLimitNs))
+            *reinterpret_cast<volatile int *>(abort_flag) = 2;
     }
     asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
     return *reinterpret_cast<volatile int *>(abort_flag) != 2;

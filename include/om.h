@@ -310,6 +310,20 @@ OM_API int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W,
  */
 OM_API int om_device_status(void *stream);
 
+/*
+ * Failure-detection self-test (the pages have no counterpart: it exists so
+ * that the timeout path of the kernels' bounded waits can be tested without
+ * a GPU fault). Launches one block on `stream` whose wait runs out after
+ * limit_ms milliseconds (1..1000): which = 0 waits on an mbarrier phase that
+ * nothing completes (the kernels' pipeline wait), which = 1 acquires a
+ * device flag that nothing sets (the balanced schedule's continuation
+ * wait). The block then records the timeout and returns; a following
+ * om_device_status(stream) reports OM_ERR_TIMEOUT (and clears it), and the
+ * context stays usable. Returns OM_OK once launched, OM_ERR_INVALID_ARG for
+ * other arguments, OM_ERR_CUDA on a launch error.
+ */
+OM_API int om_selftest_wait_timeout(int which, int limit_ms, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

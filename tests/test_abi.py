@@ -143,3 +143,8 @@ def test_epilogue_entry_points_validate_on_host(L):
                               P * 256, 0, None, 0, None) == INV
     assert L.om_conv2d_f32_ex(1, 4, 5, 5, 4, 1, 3, 3, 1, 1, 1, P, P * 64, 0, None, P * 256, 1,
                               P * 256, 0, None, 0, None) == ALIAS
+
+
+def test_selftest_hook_rejects_bad_arguments_before_launch(L):
+    for which, limit in ((2, 20), (-1, 20), (0, 0), (1, 1001)):
+        assert L.om_selftest_wait_timeout(which, limit, None) == INV
