@@ -243,6 +243,11 @@ int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, cons
     }
     if (cfg < 0) cfg = pick_gemm_cfg(p, flags != nullptr);
     cudaError_t e = om::launch_gemm_tiled(p, mode, cfg, flags, s);
+    // B rows not 16-byte aligned: A alone by TMA, same tile shape; then both
+    // operands by 4-byte copies
+    if (e == cudaErrorNotSupported)
+        e = om::launch_gemm_tiled(p, mode, cfg == om::kCfgTma128x128 ? om::kCfgMixed128x128 : om::kCfgMixed128x256,
+                                  flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_gemm_tiled(p, mode, om::kCfgAsync128x128, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_gemm_naive(p, mode, s);
     return from_cuda(e);

@@ -57,6 +57,8 @@ enum GemmCfg : int {
     kCfgAsync128x128 = 3,      // 4-byte cp.async-fed SIMT tiles (any alignment)
     kCfgTmaScalar128x256 = 4,  // as 1 with one-lane fp32 instructions
     kCfgGemv = 5,              // matrix-vector kernel (at most 8 rows or 8 columns)
+    kCfgMixed128x256 = 6,      // A by TMA, B by 4-byte cp.async (B rows not 16-byte aligned)
+    kCfgMixed128x128 = 7,      // as 6 with 128x128 tiles
 };
 
 // The matrix-vector kernels take products with at most kGemvMaxSmall rows

@@ -37,7 +37,8 @@ namespace om {
 
 __device__ unsigned g_status_gemm;
 
-enum Producer : int { kProdTma = 0, kProdAsync = 1 };
+// kProdMixed: A by TMA, B by 4-byte cp.async (B rows not 16-byte aligned).
+enum Producer : int { kProdTma = 0, kProdAsync = 1, kProdMixed = 2 };
 
 __device__ __forceinline__ void record_timeout(int *abort_flag) {
     atomicOr(&g_status_gemm, kDevErrTimeout);
@@ -139,6 +140,66 @@ __device__ __forceinline__ void produce_async(const GemmProblem &p, uint8_t *sme
     cp_async_wait_all();
 }
 
+// A by TMA (producer thread 0, with the A tile's byte count), B by 4-byte
+// cp.async from every producer thread as in produce_async; each thread's
+// copies arrive on the stage's full barrier as they land.
+template <class Cfg>
+__device__ __forceinline__ void produce_mixed(const GemmProblem &p, const CUtensorMap *mapA,
+                                              uint8_t *smem, uint64_t *full, uint64_t *empty,
+                                              int *abort_flag, const TileRaster &rs,
+                                              const Schedule &sched, int pt) {
+    constexpr int BN = Cfg::BN, BK = Cfg::BK;
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    const Schedule::Local L = sched.local();
+    for (int i = 0; i < L.count; ++i) {
+        const Segment sg = sched.at(L, i);
+        int tm, tn;
+        rs.at(sg.tile, tm, tn);
+        const int64_t n0 = static_cast<int64_t>(tn) * BN;
+        for (int kt = sg.kb; kt < sg.ke; ++kt) {
+            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                record_timeout(abort_flag);
+                cp_async_wait_all();
+                if (pt == 0) {
+                    // let the A tiles already requested land first
+                    for (int s2 = 0; s2 < Cfg::STAGES; ++s2) {
+                        if (issued > s2) {
+                            const int64_t last = s2 + ((issued - 1 - s2) / Cfg::STAGES) * Cfg::STAGES;
+                            (void)mbar_wait(&full[s2], static_cast<uint32_t>((last / Cfg::STAGES) & 1));
+                        }
+                    }
+                }
+                return;
+            }
+            ++issued;
+            uint8_t *sa = smem + stage * Cfg::STAGE_BYTES;
+            const uint32_t sb = smem_u32(sa) + Cfg::A_BYTES;
+            if (pt == 0) {
+                mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES);
+                tma_load_2d(sa, mapA, &full[stage], kt * BK, tm * Cfg::BM);
+            }
+#pragma unroll 4
+            for (int kk = 0; kk < BK; ++kk) {
+                const int64_t krow = static_cast<int64_t>(kt) * BK + kk;
+#pragma unroll
+                for (int c = pt; c < BN; c += kProducerThreads) {
+                    const int64_t col = n0 + c;
+                    const bool ok = (krow < p.k) && (col < p.n);
+                    cp_async_4_if(sb + (kk * BN + c) * 4, ok ? p.B + krow * p.ldb + col : p.B, ok);
+                }
+            }
+            cp_async_arrive_noinc(&full[stage]);
+            if (++stage == Cfg::STAGES) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+    }
+    cp_async_wait_all();
+}
+
 // Moves this thread's outputs of a tile between registers and C.
 // OP 0: final store (canonical NaN); 1: raw store of an early part's
 // accumulators; 2: load of the accumulators an earlier CTA stored.
@@ -214,7 +275,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
-            mbar_init(&full[s], PROD == kProdTma ? 1 : kProducerThreads);
+            mbar_init(&full[s], PROD == kProdTma ? 1 : kProducerThreads + (PROD == kProdMixed ? 1 : 0));
             mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
         }
         *abort_flag = 0;
@@ -231,6 +292,10 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
                 prefetch_tensormap(&mapB);
                 produce_tma<Cfg>(&mapA, &mapB, smem, full, empty, abort_flag, rs, sched);
             }
+        } else if constexpr (PROD == kProdMixed) {
+            if (threadIdx.x == Cfg::CONSUMERS) prefetch_tensormap(&mapA);
+            produce_mixed<Cfg>(p, &mapA, smem, full, empty, abort_flag, rs, sched,
+                               threadIdx.x - Cfg::CONSUMERS);
         } else {
             produce_async<Cfg>(p, smem, full, empty, abort_flag, rs, sched,
                                threadIdx.x - Cfg::CONSUMERS);
@@ -327,6 +392,13 @@ static bool tma_eligible(const GemmProblem &p) {
     return true;
 }
 
+// A alone can come by TMA (the mixed producer).
+static bool tma_eligible_a(const GemmProblem &p) {
+    if ((reinterpret_cast<uintptr_t>(p.A) & 15) != 0 || (p.lda % 4) != 0) return false;
+    if (p.m > 0x7FFFFFFF || p.n > 0x7FFFFFFF || p.k > 0x7FFFFFFF) return false;
+    return p.lda * 4 < (int64_t(1) << 40);
+}
+
 template <int MODE, class Cfg, int PROD>
 static cudaError_t launch_cfg(const GemmProblem &p, unsigned *flags, cudaStream_t s) {
     auto kernel = sgemm_tiled_kernel<MODE, Cfg, PROD>;
@@ -337,6 +409,9 @@ static cudaError_t launch_cfg(const GemmProblem &p, unsigned *flags, cudaStream_
         if (!tma_eligible(p)) return cudaErrorNotSupported;
         if (!make_map_2d(&mapA, p.A, p.m, p.k, p.lda, Cfg::BK, Cfg::BM, true)) return cudaErrorNotSupported;
         if (!make_map_2d(&mapB, p.B, p.k, p.n, p.ldb, Cfg::BN, Cfg::BK, false)) return cudaErrorNotSupported;
+    } else if constexpr (PROD == kProdMixed) {
+        if (!tma_eligible_a(p)) return cudaErrorNotSupported;
+        if (!make_map_2d(&mapA, p.A, p.m, p.k, p.lda, Cfg::BK, Cfg::BM, true)) return cudaErrorNotSupported;
     }
     const int64_t tm = (p.m + Cfg::BM - 1) / Cfg::BM, tn = (p.n + Cfg::BN - 1) / Cfg::BN;
     if (tm * tn > 0x7FFFFFFF || p.k > 0x7FFFFFFF) return cudaErrorNotSupported;
@@ -365,6 +440,8 @@ static cudaError_t launch_mode(const GemmProblem &p, int cfg, unsigned *flags, c
         case kCfgTma128x128: return launch_cfg<MODE, Cfg128x128, kProdTma>(p, flags, s);
         case kCfgAsync128x128: return launch_cfg<MODE, Cfg128x128, kProdAsync>(p, flags, s);
         case kCfgTmaScalar128x256: return launch_cfg<MODE, Cfg128x256Scalar, kProdTma>(p, flags, s);
+        case kCfgMixed128x256: return launch_cfg<MODE, Cfg128x256, kProdMixed>(p, flags, s);
+        case kCfgMixed128x128: return launch_cfg<MODE, Cfg128x128, kProdMixed>(p, flags, s);
         default: return cudaErrorNotSupported;
     }
 }

@@ -15,8 +15,9 @@ from tests.gpu_util import (assert_bits_equal, bits, forced_config, guarded_outp
 pytestmark = pytest.mark.gpu
 
 MODES = [(oracle.EXACT, "exact"), (oracle.FAST, "fast")]
-# naive, TMA 128x256, TMA 128x128, cp.async 128x128, TMA 128x256 one-lane, default
-CFGS = [0, 1, 2, 3, 4, None]
+# naive, TMA 128x256, TMA 128x128, cp.async 128x128, TMA 128x256 one-lane,
+# A by TMA and B by cp.async 128x256 and 128x128, default
+CFGS = [0, 1, 2, 3, 4, 6, 7, None]
 
 
 @pytest.fixture(scope="module", autouse=True)
