@@ -387,6 +387,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         if hbm_bound:
             extras[name].update(hbm_fields(4.0 * (c.x.size + c.w.size + c.N * c.Cout * OH * OW), t))
 
+    def chain_line(name, mode):
+        """ResNet-50's 53 convolutions at 224 x 224, batch 1, each with its
+        bias / shortcut / ReLU epilogue: one CUDA-graph replay per step, and
+        the same chain called layer by layer from the host."""
+        from implicit_gemm_convolution_gb300 import chain
+        ch = chain.ConvChain(chain.resnet50_convs(), 1, 224, mode, device=dev)
+        graph = ch.capture()
+        t_graph = float(np.median(time_calls(graph.replay, args.extra_steps, 3, flush, stream)))
+        t_eager = float(np.median(time_calls(ch.run, args.extra_steps, 3, flush, stream)))
+        tf = ch.flops / (t_graph * 1e-3) / 1e12
+        pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
+        extras[name] = {"ms": round(t_graph, 4), "ms_eager_host_calls": round(t_eager, 4),
+                        "GFLOP/s": round(tf * 1e3, 1), "roofline_frac": round(tf / pk, 4),
+                        "peak_tflops": round(pk, 2), "layers": len(ch.layers),
+                        "gflop": round(ch.flops / 1e9, 3),
+                        "context": "the pages' ResNet-50 convolution chain, 16/32 CPU threads on a "
+                                   "16-core Zen 4: 12.3/11.1 ms (other hardware)"}
+
     if not args.headline_only:
         gemm_line("gemm_4096^3_fast_ws", "fast", case, use_ws=True)
         gemm_line("gemm_4096^3_exact_no_workspace", "exact", case)
@@ -413,6 +431,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                       hbm_bound=True)
             gemm_line(f"gemm_decode_1x11008x4096_{md}", md, synth.workload_gemm_decode(),
                       hbm_bound=True)
+        for md in ("exact", "fast"):
+            chain_line(f"resnet50_conv_chain_b1_224_{md}", md)
 
     cpu = cpu_baseline(args.cpu_seconds)
     line = {
