@@ -44,6 +44,9 @@ struct DirectGeom {
     int WR, Wp;  // window rows (for R output rows) and columns
     int wfloats, tints;  // weight floats and table ints, each a multiple of 4
     int wshift;          // depthwise window: column j holds input column j - wshift
+    int R_chunk;         // few-pixel kernel: input channels per chunk
+    int ch_win, ch_w;    // few-pixel kernel: window and weight floats of one chunk buffer
+    uint32_t plane_magic;  // few-pixel kernel: floor(2^32 / (WR*Wp)) + 1
     Epilogue ep;
 };
 
@@ -157,6 +160,128 @@ __global__ void __launch_bounds__(kDirectThreads) conv_direct_kernel(const Direc
                     *o = canonical_nan(v);
                 }
             }
+        }
+    }
+}
+
+// ------------------------------------------------------- few output pixels
+// Convolutions with many output channels and few output pixels (a late
+// layer at a small batch: 512 channels of 7 x 7 outputs), where the
+// implicit-GEMM tiles would leave most SMs idle and k cannot be split. A
+// block owns MB output channels of one group, one image and a band of output
+// rows with at most kSkinnyThreads pixels; each thread owns one pixel and
+// its MB outputs for the whole k loop. The group's input channels stream
+// through shared memory in chunks of CC channels (window rows with the zero
+// border written at copy time, the chunk's weights), double-buffered with
+// cp.async groups so the next chunk's copy overlaps this chunk's taps. Taps
+// run chunk by chunk, in (c, ky, kx) order within a chunk: the pages' one
+// sequential loop per output.
+constexpr int kSkinnyThreads = 128;
+
+template <int MODE, int MB>
+__global__ void __launch_bounds__(kSkinnyThreads) conv_skinny_kernel(const DirectGeom g) {
+    extern __shared__ float4 smem4[];
+    float *base = reinterpret_cast<float *>(smem4);
+    const int buf_floats = g.ch_win + g.ch_w;  // window + weights of one buffer (multiples of 4)
+    int *tab = reinterpret_cast<int *>(base + 2 * buf_floats);
+    int *ftab = tab + g.R_chunk * g.KH * g.KW;  // per window element of a channel: input offset or -1
+    const int mblocks = (g.M + MB - 1) / MB;
+    const int grp = blockIdx.y / mblocks;
+    const int oc0 = (blockIdx.y - grp * mblocks) * MB;
+    const int64_t img = blockIdx.z;
+    const int oy0 = blockIdx.x * g.R;
+    const int rows = min(g.R, g.OH - oy0);
+    const int wr = (rows - 1) * g.sH + (g.KH - 1) * g.dH + 1;
+    const int iy_base = oy0 * g.sH - g.pT;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int taps = g.KH * g.KW;
+    const int cc_max = g.R_chunk;  // channels per chunk
+    const int nchunks = (g.cin_g + cc_max - 1) / cc_max;
+
+    // tap table of a chunk: offset of (c, ky, kx) in the chunk's window
+    for (int t = tid; t < cc_max * taps; t += kSkinnyThreads) {
+        const int c = t / taps, rr = t - (t / taps) * taps;
+        const int ky = rr / g.KW, kx = rr - (rr / g.KW) * g.KW;
+        tab[t] = (c * g.WR + ky * g.dH) * g.Wp + kx * g.dW;
+    }
+    // window element (r, j) of a channel: input offset iy*W + ix of the
+    // band's plane position, or -1 outside the plane (and past this band's rows)
+    const int plane = g.WR * g.Wp;
+    for (int e = tid; e < plane; e += kSkinnyThreads) {
+        const int r = e / g.Wp, j = e - (e / g.Wp) * g.Wp;
+        const int iy = iy_base + r, ix = j - g.pL;
+        const bool ok = r < wr && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
+                        static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
+        ftab[e] = ok ? iy * g.W + ix : -1;
+    }
+    __syncthreads();
+    const float *xg = g.x + (img * g.Cin + static_cast<int64_t>(grp) * g.cin_g) * g.HW;
+    const float *wg = g.w + static_cast<int64_t>(grp * g.M + oc0) * g.w_ld;
+    const uint32_t magic = g.plane_magic;  // e / plane == umulhi(e, magic) for e, plane < 2^16
+    auto load_chunk = [&](int ch, int b) {
+        float *win = base + b * buf_floats;
+        float *wsm = win + g.ch_win;
+        const uint32_t win32 = smem_u32(win), w32 = smem_u32(wsm);
+        const int c0 = ch * cc_max, cc = min(cc_max, g.cin_g - c0);
+        const float *xc0 = xg + static_cast<int64_t>(c0) * g.HW;
+        for (int e = tid; e < cc * plane; e += kSkinnyThreads) {
+            const int c = static_cast<int>(__umulhi(static_cast<uint32_t>(e), magic));
+            const int off = ftab[e - c * plane];
+            const bool ok = off >= 0;
+            cp_async_4_if(win32 + e * 4u, ok ? xc0 + (static_cast<int64_t>(c) * g.HW + off) : g.x, ok);
+        }
+        // weights: tap t of the chunk for channel oc at wsm[t*MB + oc], +0 past M
+        const int ntap = cc * taps;
+        for (int i = tid; i < ntap * MB; i += kSkinnyThreads) {
+            const int t = i / MB, oc = i - (i / MB) * MB;
+            const bool ok = oc0 + oc < g.M;
+            cp_async_4_if(w32 + i * 4u, ok ? wg + static_cast<int64_t>(oc) * g.w_ld + c0 * taps + t : g.w, ok);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    const int ry = tid / g.OW, ox = tid - (tid / g.OW) * g.OW;
+    const bool active = tid < rows * g.OW;
+    const int woff = (ry * g.sH) * g.Wp + ox * g.sW;
+    float2 acc[(MB + 1) / 2];
+    float acc1 = 0.0f;
+#pragma unroll
+    for (int h = 0; h < (MB + 1) / 2; ++h) acc[h] = make_float2(0.0f, 0.0f);
+
+    load_chunk(0, 0);
+    for (int ch = 0; ch < nchunks; ++ch) {
+        const int b = ch & 1;
+        if (ch + 1 < nchunks) {
+            load_chunk(ch + 1, b ^ 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        if (active) {
+            const float *win = base + b * buf_floats;
+            const float *wsm = win + g.ch_win;
+            const int ntap = min(cc_max, g.cin_g - ch * cc_max) * taps;
+            const float *src = win + woff;
+#pragma unroll 4
+            for (int t = 0; t < ntap; ++t) direct_tap<MODE, MB>(acc, acc1, wsm + t * MB, src[tab[t]]);
+        }
+        __syncthreads();  // the buffer is refilled two chunks on
+    }
+    if (!active) return;
+    const int oy = oy0 + ry;
+    float *yp = g.y + (img * g.Cout + static_cast<int64_t>(grp) * g.M + oc0) * g.P +
+                static_cast<int64_t>(oy) * g.OW + ox;
+    const bool ep = g.ep.bias || g.ep.res || g.ep.act;
+#pragma unroll
+    for (int oc = 0; oc < MB; ++oc) {
+        if (oc0 + oc < g.M) {
+            float v = MB == 1 ? acc1 : ((oc & 1) ? acc[oc / 2].y : acc[oc / 2].x);
+            float *o = yp + static_cast<int64_t>(oc) * g.P;
+            if (ep)
+                v = epilogue_value(v, g.ep.bias ? g.ep.bias + grp * g.M + oc0 + oc : nullptr,
+                                   g.ep.res ? g.ep.res + (o - g.y) : nullptr, g.ep.act);
+            *o = canonical_nan(v);
         }
     }
 }
@@ -350,6 +475,31 @@ cudaError_t launch_direct_mode(const DirectGeom &g, int64_t groups, int64_t imag
     }
 }
 
+template <int MODE, int MB>
+cudaError_t launch_skinny(const DirectGeom &g, int64_t bands, int64_t gy, int64_t images, size_t smem,
+                          cudaStream_t s) {
+    auto kernel = conv_skinny_kernel<MODE, MB>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3(static_cast<unsigned>(bands), static_cast<unsigned>(gy), static_cast<unsigned>(images)),
+             kSkinnyThreads, smem, s>>>(g);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_skinny_mb(const DirectGeom &g, int mb, int64_t bands, int64_t gy, int64_t images,
+                             size_t smem, cudaStream_t s) {
+    switch (mb) {
+        case 1: return launch_skinny<MODE, 1>(g, bands, gy, images, smem, s);
+        case 2: return launch_skinny<MODE, 2>(g, bands, gy, images, smem, s);
+        case 4: return launch_skinny<MODE, 4>(g, bands, gy, images, smem, s);
+        case 8: return launch_skinny<MODE, 8>(g, bands, gy, images, smem, s);
+        case 16: return launch_skinny<MODE, 16>(g, bands, gy, images, smem, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 }  // namespace
 
 int conv_direct_channels(int64_t M) {
@@ -480,6 +630,71 @@ cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s) {
     const int pxi = static_cast<int>(px);
     return mode == kFast ? launch_direct_mode<kFast>(g, p.G, p.N, mb, pxi, smem, s)
                          : launch_direct_mode<kExact>(g, p.G, p.N, mb, pxi, smem, s);
+}
+
+}  // namespace om
+
+namespace om {
+
+cudaError_t launch_conv_skinny(const ConvProblem &p, int mode, cudaStream_t s) {
+    if (p.N == 0 || p.OH * p.OW == 0) return cudaSuccess;
+    const int64_t M = p.Cout / p.G, cin_g = p.Cin / p.G, taps = p.KH * p.KW;
+    // one output pixel per thread: bands of whole output rows, at most
+    // kSkinnyThreads pixels each; 32-bit offsets with room to spare
+    constexpr int64_t kCoordMax = int64_t{1} << 24;
+    if (p.OW > kSkinnyThreads || p.H > kCoordMax || p.W > kCoordMax || p.pT > kCoordMax ||
+        p.pL > kCoordMax || p.sH > kCoordMax || p.sW > kCoordMax || p.dH * p.KH > kCoordMax ||
+        p.dW * p.KW > kCoordMax || p.N > 65535 || p.w_ld > 0x7FFFFFFF ||
+        p.Cin * p.H * p.W > 0x7FFFFFFF || p.Cout * p.OH * p.OW > 0x7FFFFFFF || p.K > 0x7FFFFFFF)
+        return cudaErrorNotSupported;
+    const int64_t R = std::min<int64_t>(p.OH, kSkinnyThreads / p.OW);
+    const int64_t bands = (p.OH + R - 1) / R;
+    const int64_t WR = (R - 1) * p.sH + (p.KH - 1) * p.dH + 1;
+    const int64_t Wp = (p.OW - 1) * p.sW + (p.KW - 1) * p.dW + 1;
+    // output channels per thread (up to 16): the most that still give every
+    // SM a block. Each block streams the whole input window, so fewer blocks
+    // with more channels each read less from L2 (measured on ResNet-50's
+    // late layers: one block per SM beat two, and 16 channels beat 8).
+    const int64_t want = static_cast<int64_t>(num_sms());
+    int mb = 1;
+    for (int c = 2; c <= 16; c *= 2)
+        if (bands * p.G * ((M + c - 1) / c) * p.N >= want) mb = c;
+    const int64_t gy = p.G * ((M + mb - 1) / mb);
+    if (gy > 65535) return cudaErrorNotSupported;
+    // channels per chunk: two buffers of (window + weights) and one tap table
+    // in 48 KB; window and weights each rounded up to 4 floats, so that the
+    // weights' 8- and 16-byte loads stay aligned in both buffers
+    auto round4 = [](int64_t v) { return (v + 3) / 4 * 4; };
+    const int64_t plane = WR * Wp;
+    if (plane >= (1 << 15)) return cudaErrorNotSupported;
+    const int64_t per_channel = 2 * (plane + taps * mb) + taps;
+    int64_t cc = std::min<int64_t>(cin_g, (48 * 1024 / 4 - 32 - plane) / per_channel);
+    if (cc < 1) return cudaErrorNotSupported;
+    auto floats = [&](int64_t c) { return 2 * (round4(c * plane) + round4(c * taps * mb)) + c * taps + plane; };
+    while (cc > 1 && floats(cc) > 48 * 1024 / 4) --cc;
+    if (floats(cc) > 48 * 1024 / 4 || cc * plane >= (1 << 16)) return cudaErrorNotSupported;
+    DirectGeom g{};
+    g.x = p.x; g.w = p.w; g.y = p.y;
+    g.H = static_cast<int>(p.H); g.W = static_cast<int>(p.W); g.HW = static_cast<int>(p.H * p.W);
+    g.OH = static_cast<int>(p.OH); g.OW = static_cast<int>(p.OW); g.P = static_cast<int>(p.OH * p.OW);
+    g.Cin = static_cast<int>(p.Cin); g.Cout = static_cast<int>(p.Cout);
+    g.cin_g = static_cast<int>(cin_g); g.M = static_cast<int>(M);
+    g.K = static_cast<int>(p.K); g.w_ld = static_cast<int>(p.w_ld);
+    g.KH = static_cast<int>(p.KH); g.KW = static_cast<int>(p.KW);
+    g.sH = static_cast<int>(p.sH); g.sW = static_cast<int>(p.sW);
+    g.pT = static_cast<int>(p.pT); g.pL = static_cast<int>(p.pL);
+    g.dH = static_cast<int>(p.dH); g.dW = static_cast<int>(p.dW);
+    g.R = static_cast<int>(R);
+    g.WR = static_cast<int>(WR);
+    g.Wp = static_cast<int>(Wp);
+    g.R_chunk = static_cast<int>(cc);
+    g.ch_win = static_cast<int>(round4(cc * WR * Wp));
+    g.ch_w = static_cast<int>(round4(cc * taps * mb));
+    g.ep = p.ep;
+    g.plane_magic = static_cast<uint32_t>((uint64_t{1} << 32) / static_cast<uint64_t>(plane) + 1);
+    const size_t smem = static_cast<size_t>(floats(cc)) * 4;
+    return mode == kFast ? launch_skinny_mb<kFast>(g, mb, bands, gy, p.N, smem, s)
+                         : launch_skinny_mb<kExact>(g, mb, bands, gy, p.N, smem, s);
 }
 
 }  // namespace om

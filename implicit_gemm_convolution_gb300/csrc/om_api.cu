@@ -159,6 +159,14 @@ int pick_gemm_cfg(const GemmProblem &p, bool balanced) {
     return c128 < c256 ? om::kCfgTma128x128 : om::kCfgTma128x256;
 }
 
+// The implicit GEMM's 64 x 256 tiles would not give every SM a tile, and the
+// k loop is long: the few-pixel kernel keeps one output pixel per thread.
+bool few_pixels(const ConvProblem &p) {
+    const int64_t M = p.Cout / p.G;
+    const int64_t tiles = p.G * ((M + 63) / 64) * ((p.N * p.OH * p.OW + 255) / 256);
+    return tiles < om::num_sms() && p.K >= 64 && p.OW <= 128;
+}
+
 int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     const int cfg = forced("OM_FORCE_CONV_CFG");
     if (cfg == om::kConvNaive || p.K == 0) return from_cuda(om::launch_conv_naive(p, mode, s));
@@ -167,7 +175,10 @@ int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     if (e == cudaErrorNotSupported &&
         (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM)))
         e = om::launch_conv_direct(p, mode, s);
-    if (e == cudaErrorNotSupported && cfg != om::kConvDirect && cfg != om::kConvGemv)
+    if (e == cudaErrorNotSupported && (cfg == om::kConvSkinny || (cfg < 0 && few_pixels(p))))
+        e = om::launch_conv_skinny(p, mode, s);
+    if (e == cudaErrorNotSupported && cfg != om::kConvDirect && cfg != om::kConvGemv &&
+        cfg != om::kConvSkinny)
         e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
     return from_cuda(e);

@@ -72,6 +72,7 @@ enum ConvCfg : int {
     kConvImplicit = 1,  // implicit GEMM with gathered patches, 64 x 256 tiles
     kConvDirect = 2,    // one thread per output pixel and group, all of its channels
     kConvGemv = 3,      // 1x1 over a 1x1 input: matrix-vector kernel
+    kConvSkinny = 4,    // few output pixels: one pixel per thread, channels streamed in chunks
 };
 
 // The direct kernel serves groups of up to kConvDirectMaxM output channels
@@ -84,6 +85,8 @@ constexpr int kConvDirectAutoM = 16;
 // (M rounded up to a power of two), or 0 above kConvDirectMaxM.
 int conv_direct_channels(int64_t M);
 cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s);
+// Few output pixels (output rows of at most 128 pixels), many output channels.
+cudaError_t launch_conv_skinny(const ConvProblem &p, int mode, cudaStream_t s);
 
 // Matrix-vector kernels; cudaErrorNotSupported when the shape is not theirs.
 cudaError_t launch_gemm_gemv(const GemmProblem &p, int mode, cudaStream_t s);

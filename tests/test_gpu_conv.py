@@ -11,7 +11,7 @@ from tests.gpu_util import (assert_bits_equal, forced_config, guarded_output, gu
 pytestmark = pytest.mark.gpu
 
 MODES = [(oracle.EXACT, "exact"), (oracle.FAST, "fast")]
-CFGS = [0, 1, 2, None]  # naive, implicit GEMM, direct small-group kernel, default dispatch
+CFGS = [0, 1, 2, 4, None]  # naive, implicit GEMM, direct small-group, few-pixel kernel, default
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -96,6 +96,13 @@ SMALL = [
     # rows a multiple of 4 floats (16-byte window copies and stores)
     (2, 8, 20, 32, 8, 8, 5, 5, 2, 2, 1),
     (2, 8, 30, 64, 8, 8, 3, 3, 2, 1, 1),
+    # few output pixels, many output channels (the few-pixel kernel with 2 and
+    # 4 channels per thread; a 9 x 9 window per channel, so an odd-sized
+    # chunk window before the weights)
+    (2, 9, 7, 7, 512, 1, 3, 3, 1, 1, 1),
+    (4, 9, 7, 7, 512, 1, 3, 3, 1, 1, 1),
+    (1, 300, 7, 7, 64, 1, 3, 3, 1, 1, 1),
+    (8, 40, 7, 7, 1024, 1, 1, 1, 1, 0, 1),
 ]
 
 
