@@ -432,6 +432,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             gemm_line(f"gemm_decode_1x11008x4096_{md}", md, synth.workload_gemm_decode(),
                       hbm_bound=True)
         for md in ("exact", "fast"):
+            conv_line(f"conv_late3x3_n1_c512_7_{md}", md, synth.workload_conv_late3x3())
+        for md in ("exact", "fast"):
             chain_line(f"resnet50_conv_chain_b1_224_{md}", md)
 
     cpu = cpu_baseline(args.cpu_seconds)
@@ -542,7 +544,8 @@ def run_profile(args):
              "gemm_decode": synth.workload_gemm_decode}
     convs = {"conv3x3": synth.workload_conv3x3, "conv1x1": synth.workload_conv1x1,
              "conv_grouped": synth.workload_conv_grouped,
-             "conv_depthwise": synth.workload_conv_depthwise}
+             "conv_depthwise": synth.workload_conv_depthwise,
+             "conv_late3x3": synth.workload_conv_late3x3}
     if name in gemms:
         case = gemms[name]()
         A = torch.from_numpy(case.A).to(dev)
@@ -588,8 +591,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--profile", default=None,
                     help="workload:mode (gemm_4096^3, gemm_prefill, gemm_prefill_ragged, gemm_decode,"
-                         " conv3x3, conv1x1, conv_grouped, conv_depthwise) -- launch only that"
-                         " kernel, for ncu")
+                         " conv3x3, conv1x1, conv_grouped, conv_depthwise, conv_late3x3) -- launch"
+                         " only that kernel, for ncu")
     args = ap.parse_args()
     if args.profile:
         run_profile(args)

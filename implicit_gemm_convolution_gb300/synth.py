@@ -274,3 +274,9 @@ def workload_conv_depthwise() -> ConvCase:
 def workload_gemm_decode() -> GemmCase:
     return make_gemm("gemm_decode_1x11008x4096", 1, 11008, 4096, seed=8,
                      dist_a=("normal", 0.0, 1.0), dist_b=("normal", 0.0, 0.02))
+
+
+def workload_conv_late3x3() -> ConvCase:
+    """A late ResNet-50 layer at batch 1: 512 -> 512 channels, 3x3, 7x7 (49 output pixels)."""
+    return make_conv("conv_late3x3_n1_c512_7", 1, 512, 7, 7, 512, 1, 3, 3, 1, 1, 1, seed=10,
+                     dist_x=("uniform", 0.0, 1.0), dist_w=("normal", 0.0, math.sqrt(2.0 / 4608)))
