@@ -299,10 +299,59 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             raise RuntimeError("om_gemm_f32 failed")
         hC.copy_(C, non_blocking=True)
 
-    e2e_ms = float(np.mean(time_calls(e2e_step, max(2, args.steps // 2), 2, flush, stream)))
+    serial_ms = float(np.mean(time_calls(e2e_step, max(2, args.steps // 2), 2, flush, stream)))
+
+    # Pipelined over steps: two device buffer sets; step i's host-to-device
+    # copies (one stream) and step i-1's result read-back (another) overlap
+    # step i-1's / i's product. Every step still copies its inputs in and its
+    # result out inside the timed region.
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    sets = [(torch.empty_like(A), torch.empty_like(B), torch.empty_like(C),
+             torch.empty((m, n), dtype=torch.float32).pin_memory()) for _ in range(2)]
+
+    def run_pipelined(steps):
+        free = [None, None]  # event: the set's last read-back finished
+        for i in range(steps):
+            dA_, dB_, C_, hC_ = sets[i % 2]
+            if free[i % 2] is not None:
+                h2d.wait_event(free[i % 2])
+            with torch.cuda.stream(h2d):
+                dA_.copy_(hA, non_blocking=True)
+                dB_.copy_(hB, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(h2d)
+            stream.wait_event(ready)
+            st = om.gemm_raw(m, n, k, dA_.data_ptr(), k, dB_.data_ptr(), n, C_.data_ptr(), n,
+                             "exact", stream, workspace=ws)
+            if st != 0:
+                raise RuntimeError("om_gemm_f32 failed")
+            computed = torch.cuda.Event()
+            computed.record(stream)
+            d2h.wait_event(computed)
+            with torch.cuda.stream(d2h):
+                hC_.copy_(C_, non_blocking=True)
+            free[i % 2] = torch.cuda.Event()
+            free[i % 2].record(d2h)
+        stream.wait_stream(h2d)
+        stream.wait_stream(d2h)
+
+    run_pipelined(3)
+    torch.cuda.synchronize()
+    e2e_steps = max(4, args.steps // 2)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    run_pipelined(e2e_steps)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = p0.elapsed_time(p1) / e2e_steps
     e2e = {"value": round(flops / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
            "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
-           "d2h_bytes_per_step": int(hC.numel() * 4), "ms_per_step": round(e2e_ms, 4)}
+           "d2h_bytes_per_step": int(hC.numel() * 4), "ms_per_step": round(e2e_ms, 4),
+           "steps": e2e_steps,
+           "how": "pinned host A, B in and C out every step, on two copy streams that overlap "
+                  "the neighbouring steps' products (two device buffer sets)",
+           "serial_ms_per_step": round(serial_ms, 4),
+           "serial_value": round(flops / (serial_ms * 1e-3) / 1e9, 1)}
 
     # ---- per-mode and per-workload lines (same timing rules)
     extras = {}
