@@ -5,9 +5,9 @@
 // separate tolerance mode with a stated bound:
 //   |C - C_exact| <= 1e-5 * sqrt(k) * sum_p |A[i][p]| * |B[p][j]|
 // for outputs whose exact-mode result is finite. Each operand value x is
-// split into x_hi = tf32(x) (round to nearest, ties away) and
-// x_lo = tf32(x - x_hi); the product a*b is taken as
-// a_lo*b_hi + a_hi*b_lo + a_hi*b_hi (a_lo*b_lo, about 2^-22 |ab|, is
+// split into x_hi = x truncated to TF32 and x_lo = tf32(x - x_hi) (round to
+// nearest, ties away); the product a*b is taken as
+// a_lo*b_hi + a_hi*b_lo + a_hi*b_hi (a_lo*b_lo, below 2^-20 |ab|, is
 // dropped), accumulated in fp32 in tensor memory in the tensor core's own
 // order. NaN results are stored as 0x7FC00000 like the exact modes.
 //
@@ -89,18 +89,17 @@ __device__ __forceinline__ void fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// TF32 split of one value: hi = tf32(a), lo = tf32(a - hi); lo = 0 when hi is
-// not finite; a finite value whose rounding would overflow is truncated.
+// TF32 split of one value: hi = a truncated to TF32 (round toward zero, so a
+// finite value never overflows), lo = tf32(a - hi) (a - hi is exact in fp32);
+// lo = 0 when hi is not finite.
 __device__ __forceinline__ void split(float a, float &hi, float &lo) {
     uint32_t h;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(a));
-    float fh = __uint_as_float(h);
-    if (isinf(fh) && !isinf(a)) fh = __uint_as_float(__float_as_uint(a) & 0xFFFFE000u);
-    const float r = __fsub_rn(a, fh);
+    asm("cvt.rz.tf32.f32 %0, %1;" : "=r"(h) : "f"(a));
+    const float fh = __uint_as_float(h);
     uint32_t l;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(r));
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(__fsub_rn(a, fh)));
     hi = fh;
-    lo = isfinite(fh) ? __uint_as_float(l) : 0.0f;
+    lo = fabsf(fh) < INFINITY ? __uint_as_float(l) : 0.0f;
 }
 
 // Explicit shared-memory accesses on 32-bit shared addresses.
