@@ -43,7 +43,10 @@ constexpr int S_OPS = 2;                     // converted operand stages
 constexpr int TILE_BYTES = 128 * 32 * 4;     // 16 KB: any 128 x 32 fp32 tile
 constexpr int F32_STAGE = 2 * TILE_BYTES;    // A, B
 constexpr int OPS_STAGE = 4 * TILE_BYTES;    // A_hi, A_lo, B_hi, B_lo
-constexpr int kConvWarps = 16;  // measured: 8 -> 12 -> 16 warps gave 126 -> 141 -> 147 TFLOP/s
+// measured: 8 -> 12 -> 16 warps gave 126 -> 141 -> 147 TFLOP/s with the
+// rounding split; with the truncating split 12, 16, 20 and 24 warps give
+// 200, 202, 198 and 189 TFLOP/s
+constexpr int kConvWarps = 16;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kFirstConvWarp = 2;
 constexpr int kFirstEpiWarp = kFirstConvWarp + kConvWarps;  // 18
