@@ -108,9 +108,12 @@ OM_API int64_t om_conv_out_dim(int64_t size, int64_t ksize, int64_t stride, int6
  * k > 0, ldb when k > 0, ldc always for a non-empty C).
  * Any 4-byte alignment of A, B, C and any lda, ldb, ldc is accepted; 16-byte
  * aligned operands with lda, ldb multiples of 4 take the TMA-fed kernel,
- * others a kernel fed by 4-byte copies; both give identical bits.
- * OM_MODE_TF32X3: each operand is split into a TF32 high part and a TF32
- * low part; C accumulates hi*hi + hi*lo + lo*hi in fp32 on the tensor cores.
+ * others a kernel fed by TMA for A and 4-byte copies for B, or by 4-byte
+ * copies for both; products with at most 8 rows or 8 columns run as
+ * matrix-vector products. Every path gives identical bits.
+ * OM_MODE_TF32X3: each operand is split into a TF32 high part (truncated)
+ * and a TF32 low part (the rounded remainder); C accumulates
+ * hi*hi + hi*lo + lo*hi in fp32 on the tensor cores.
  * Bound, for outputs whose exact-mode result is finite:
  *   |C - C_exact| <= 1e-5 * sqrt(k) * sum_p |A[i][p]| * |B[p][j]|.
  * Non-finite inputs give non-finite outputs where the exact result is
@@ -192,7 +195,13 @@ OM_API int om_gemm_f32_no_alloc(int64_t m, int64_t n, int64_t k,
  * matrix product: per image and group, A = the group's weights
  * (Cout/G x Cin/G*KH*KW), B = the input patches gathered straight into
  * on-chip memory with the zero border written during the gather, C = the
- * group's output planes. Padding is never materialised.
+ * group's output planes. Padding is never materialised. Shapes the
+ * implicit product would run poorly go to other kernels with the same
+ * per-output loop and the same bits: groups of at most 16 output channels
+ * (depthwise included) and layers with few output pixels run from input
+ * windows staged in on-chip memory (zero border written at copy time), and a
+ * 1x1 kernel over a 1x1 input of at most 8 images runs as a matrix-vector
+ * product.
  *   x: [N][Cin][H][W] contiguous.
  *   w: [Cout][Cin/G][KH][KW] contiguous.
  *   y: [N][Cout][OutH][OutW] contiguous, OutH/OutW from om_conv_out_dim.
