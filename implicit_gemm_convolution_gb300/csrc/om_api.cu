@@ -175,10 +175,12 @@ int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     if (e == cudaErrorNotSupported &&
         (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM)))
         e = om::launch_conv_direct(p, mode, s);
+    if (e == cudaErrorNotSupported && (cfg == om::kConvColumns || (cfg < 0 && few_pixels(p))))
+        e = om::launch_conv_columns(p, mode, s);
     if (e == cudaErrorNotSupported && (cfg == om::kConvSkinny || (cfg < 0 && few_pixels(p))))
         e = om::launch_conv_skinny(p, mode, s);
     if (e == cudaErrorNotSupported && cfg != om::kConvDirect && cfg != om::kConvGemv &&
-        cfg != om::kConvSkinny)
+        cfg != om::kConvSkinny && cfg != om::kConvColumns)
         e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
     return from_cuda(e);

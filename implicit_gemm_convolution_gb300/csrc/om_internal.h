@@ -73,6 +73,7 @@ enum ConvCfg : int {
     kConvDirect = 2,    // one thread per output pixel and group, all of its channels
     kConvGemv = 3,      // 1x1 over a 1x1 input: matrix-vector kernel
     kConvSkinny = 4,    // few output pixels: one pixel per thread, channels streamed in chunks
+    kConvColumns = 5,   // blocks of 32 channels x 8 pixels, weights by TMA, patches gathered
 };
 
 // The direct kernel serves groups of up to kConvDirectMaxM output channels
@@ -91,6 +92,11 @@ cudaError_t launch_conv_skinny(const ConvProblem &p, int mode, cudaStream_t s);
 // Matrix-vector kernels; cudaErrorNotSupported when the shape is not theirs.
 cudaError_t launch_gemm_gemv(const GemmProblem &p, int mode, cudaStream_t s);
 cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s);
+// A convolution as per-image, per-group products in blocks of 32 output
+// channels by 8 output pixels (the few-columns matrix-vector kernel): 1x1
+// unpadded kernels read the input directly, others of up to 64 taps gather
+// their patches during the copy.
+cudaError_t launch_conv_columns(const ConvProblem &p, int mode, cudaStream_t s);
 cudaError_t read_clear_status_gemv(unsigned *out, cudaStream_t s);
 
 // Failure-detection self-test (selftest.cu): a one-block kernel whose

@@ -11,7 +11,7 @@ from tests.gpu_util import (assert_bits_equal, forced_config, guarded_output, gu
 pytestmark = pytest.mark.gpu
 
 MODES = [(oracle.EXACT, "exact"), (oracle.FAST, "fast")]
-CFGS = [0, 1, 2, 4, None]  # naive, implicit GEMM, direct small-group, few-pixel kernel, default
+CFGS = [0, 1, 2, 4, 5, None]  # naive, implicit GEMM, direct small-group, few-pixel, 1x1 columns, default
 
 
 @pytest.fixture(scope="module", autouse=True)
