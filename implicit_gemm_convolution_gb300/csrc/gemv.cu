@@ -453,7 +453,7 @@ cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s) {
     return launch_gemv(g, mode, false, p.G, p.Cout, p.w_ld, s);
 }
 
-cudaError_t launch_conv_columns(const ConvProblem &p, int mode, cudaStream_t s) {
+cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cudaStream_t s) {
     // per image and group, the product of the group's weights (Cout/G x K)
     // with the patch matrix (K x OH*OW) in blocks of 32 output channels by 8
     // pixels: a 1x1 unpadded kernel reads the input pixels directly (rows
@@ -469,11 +469,12 @@ cudaError_t launch_conv_columns(const ConvProblem &p, int mode, cudaStream_t s) 
                     P > (int64_t{1} << 30)))
         return cudaErrorNotSupported;
     if (P < 1) return cudaSuccess;
-    // gathered patches pay off with a long k loop and a block for every SM
+    // when choosing: gathered patches pay off with a long k loop and a block
+    // for every SM
     // (measured on ResNet-50 at batch 1: the 7x7 stem and the 512-channel 3x3
     // layers at 7x7 ran faster in the few-pixel kernel)
     const int64_t blocks = (M + kGemvOut - 1) / kGemvOut * ((P + kGemvMaxSmall - 1) / kGemvMaxSmall) * p.N * p.G;
-    if (!direct && (p.K < 256 || blocks < num_sms())) return cudaErrorNotSupported;
+    if (choose && !direct && (p.K < 256 || blocks < num_sms())) return cudaErrorNotSupported;
     GemvProblem g{};
     g.m = M; g.n = P; g.k = p.K;
     g.A = p.w; g.a_si = p.w_ld; g.a_sp = 1;

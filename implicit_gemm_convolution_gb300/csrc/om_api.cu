@@ -176,7 +176,7 @@ int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
         (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM)))
         e = om::launch_conv_direct(p, mode, s);
     if (e == cudaErrorNotSupported && (cfg == om::kConvColumns || (cfg < 0 && few_pixels(p))))
-        e = om::launch_conv_columns(p, mode, s);
+        e = om::launch_conv_columns(p, mode, cfg < 0, s);
     if (e == cudaErrorNotSupported && (cfg == om::kConvSkinny || (cfg < 0 && few_pixels(p))))
         e = om::launch_conv_skinny(p, mode, s);
     if (e == cudaErrorNotSupported && cfg != om::kConvDirect && cfg != om::kConvGemv &&

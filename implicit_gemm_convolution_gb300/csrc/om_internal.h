@@ -96,7 +96,8 @@ cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s);
 // channels by 8 output pixels (the few-columns matrix-vector kernel): 1x1
 // unpadded kernels read the input directly, others of up to 64 taps gather
 // their patches during the copy.
-cudaError_t launch_conv_columns(const ConvProblem &p, int mode, cudaStream_t s);
+// choose: decline gathered layers with a short k loop or too few blocks.
+cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cudaStream_t s);
 cudaError_t read_clear_status_gemv(unsigned *out, cudaStream_t s);
 
 // Failure-detection self-test (selftest.cu): a one-block kernel whose
