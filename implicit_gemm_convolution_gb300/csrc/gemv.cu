@@ -73,6 +73,7 @@ struct GemvProblem {
     // [R * cg, R * cg + R) of n); blockIdx.z = image, with these offsets of
     // B, C and res per image
     int col_groups, images;
+    int col_width;  // columns per column group (a power of two up to 8)
     int64_t img_b, img_c, img_res;
     // few columns, im2col: B(p, j) is tap p = (c, ky, kx) of output pixel
     // j = (oy, ox) of a convolution: x[c][oy*sH - pT + ky*dH][ox*sW - pL + kx*dW],
@@ -394,8 +395,9 @@ cudaError_t launch_gemv(GemvProblem g, int mode, bool rows, int64_t groups, int6
     if (g.col_groups < 1) g.col_groups = 1;
     if (g.images < 1) g.images = 1;
     if (g.b_jw < 1) g.b_jw = int64_t{1} << 62;  // one row: j / b_jw == 0
-    // with column groups each block takes kGemvMaxSmall columns
-    const int64_t small = rows ? g.m : (g.col_groups > 1 ? kGemvMaxSmall : g.n);
+    // with column groups each block takes col_width columns
+    if (g.col_width < 1) g.col_width = kGemvMaxSmall;
+    const int64_t small = rows ? g.m : (g.col_groups > 1 ? g.col_width : g.n);
     const int64_t big = rows ? g.n : g.m;
     if (small < 1 || small > kGemvMaxSmall || g.k < 1 || groups < 1 ||
         groups * g.col_groups > 65535 || g.images > 65535 || g.k > 0x7FFFFFFF - kGemvRS ||
@@ -469,12 +471,14 @@ cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cud
                     P > (int64_t{1} << 30)))
         return cudaErrorNotSupported;
     if (P < 1) return cudaSuccess;
+    // columns per block: 8, or fewer while that leaves SMs without a block
+    int width = kGemvMaxSmall;
+    auto blocks = [&](int w) { return (M + kGemvOut - 1) / kGemvOut * ((P + w - 1) / w) * p.N * p.G; };
+    while (width > 2 && blocks(width) < num_sms()) width /= 2;
     // when choosing: gathered patches pay off with a long k loop and a block
-    // for every SM
-    // (measured on ResNet-50 at batch 1: the 7x7 stem and the 512-channel 3x3
-    // layers at 7x7 ran faster in the few-pixel kernel)
-    const int64_t blocks = (M + kGemvOut - 1) / kGemvOut * ((P + kGemvMaxSmall - 1) / kGemvMaxSmall) * p.N * p.G;
-    if (choose && !direct && (p.K < 256 || blocks < num_sms())) return cudaErrorNotSupported;
+    // for every SM (measured on ResNet-50 at batch 1: the 7x7 stem ran faster
+    // in the few-pixel kernel)
+    if (choose && !direct && (p.K < 256 || blocks(width) < num_sms())) return cudaErrorNotSupported;
     GemvProblem g{};
     g.m = M; g.n = P; g.k = p.K;
     g.A = p.w; g.a_si = p.w_ld; g.a_sp = 1;
@@ -486,7 +490,8 @@ cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cud
     g.act = p.ep.act;
     g.grp_a = M * p.w_ld; g.grp_b = cin_g * HW; g.grp_c = M * P; g.grp_bias = M; g.grp_res = M * P;
     g.grp_map_rows = M;
-    g.col_groups = static_cast<int>(std::min<int64_t>((P + kGemvMaxSmall - 1) / kGemvMaxSmall, 65536));
+    g.col_width = width;
+    g.col_groups = static_cast<int>(std::min<int64_t>((P + width - 1) / width, 65536));
     g.images = static_cast<int>(std::min<int64_t>(p.N, 65536));
     g.img_b = p.Cin * HW; g.img_c = p.Cout * P; g.img_res = p.Cout * P;
     if (!direct) {
