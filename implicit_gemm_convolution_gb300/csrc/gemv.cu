@@ -81,7 +81,7 @@ struct GemvProblem {
     int im2col;
     int H, W, OW, KW, taps, sH, sW, pT, pL, dH, dW;
     int64_t HW;
-    uint32_t magic_taps, magic_kw;  // p / taps = umulhi(p, magic_taps) for p < 2^24; t / KW likewise
+    uint32_t magic_kw;  // t / KW = umulhi(t, magic_kw) for t < taps
 };
 
 struct GemvBlock {
@@ -126,15 +126,26 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
     const float *A = g.A + grp * g.grp_a;
     const float *B = g.B + grp * g.grp_b;
     const float *Bg = B + bl.img * g.img_b;  // this block's image
-    // im2col: input coordinates of tap (0, 0) of this lane's output pixel
-    int col_iy0 = 0, col_ix0 = 0;
-    if (!ROWS && g.im2col) {
-        const int j = bl.cg * R + lane % R;
-        const int jy = j / g.OW, jx = j - (j / g.OW) * g.OW;
-        col_iy0 = jy * g.sH - g.pT;
-        col_ix0 = jx * g.sW - g.pL;
-    }
     const int64_t n_here = ROWS ? g.n : min(static_cast<int64_t>(R), g.n - static_cast<int64_t>(bl.cg) * R);
+    // im2col: lane r copies row r of every stage (tap p = kt * 32 + r) for
+    // all R columns. Per column, the input coordinates of its tap (0, 0);
+    // per lane, its tap's channel c and position t = ky * KW + kx in the
+    // kernel, advanced by 32 taps a stage.
+    int col_iy0[R], col_ix0[R];
+    int tap_c = 0, tap_t = 0, step_c = 0, step_t = 0;
+    if (!ROWS && g.im2col) {
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int j = bl.cg * R + q;
+            const int jy = j / g.OW, jx = j - (j / g.OW) * g.OW;
+            col_iy0[q] = jy * g.sH - g.pT;
+            col_ix0[q] = jx * g.sW - g.pL;
+        }
+        tap_c = lane / g.taps;
+        tap_t = lane - tap_c * g.taps;
+        step_c = kGemvRS / g.taps;
+        step_t = kGemvRS - step_c * g.taps;
+    }
     const uint32_t base32 = smem_u32(base);
     for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % kGemvStages;
@@ -183,20 +194,24 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
         }
         // the small operand: A columns [32][R] (few rows) or B rows [32][R] (few columns)
         if (!ROWS && g.im2col) {
-            // this lane's column q = lane % R, rows r = lane / R + (32 / R) i
-            const int q = lane % R;
-            for (int r = lane / R; r < kGemvRS; r += 32 / R) {
-                const int64_t p = p0 + r;
-                const uint32_t pp = static_cast<uint32_t>(p);
-                const int c = g.taps == 1 ? static_cast<int>(pp) : static_cast<int>(__umulhi(pp, g.magic_taps));
-                const int t = static_cast<int>(pp) - c * g.taps;
-                const int ky = g.KW == 1 ? t : static_cast<int>(__umulhi(static_cast<uint32_t>(t), g.magic_kw));
-                const int kx = t - ky * g.KW;
-                const int iy = col_iy0 + ky * g.dH, ix = col_ix0 + kx * g.dW;
-                const bool ok = p < g.k && q < n_here && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
+            const bool p_ok = p0 + lane < g.k;
+            const int ky = g.KW == 1 ? tap_t
+                                     : static_cast<int>(__umulhi(static_cast<uint32_t>(tap_t), g.magic_kw));
+            const int dy = ky * g.dH, dx = (tap_t - ky * g.KW) * g.dW;
+            const float *plane = Bg + (p_ok ? static_cast<int64_t>(tap_c) * g.HW : 0);
+#pragma unroll
+            for (int q = 0; q < R; ++q) {
+                const int iy = col_iy0[q] + dy, ix = col_ix0[q] + dx;
+                const bool ok = p_ok && q < n_here && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
                                 static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
-                const float *src = ok ? Bg + (static_cast<int64_t>(c) * g.HW + static_cast<int64_t>(iy) * g.W + ix) : Bg;
-                cp_async_4_if(small32 + (r * R + q) * 4, src, ok);
+                const float *src = ok ? plane + (static_cast<int64_t>(iy) * g.W + ix) : Bg;
+                cp_async_4_if(small32 + (lane * R + q) * 4, src, ok);
+            }
+            tap_c += step_c;
+            tap_t += step_t;
+            if (tap_t >= g.taps) {
+                tap_t -= g.taps;
+                ++tap_c;
             }
         } else
         for (int e = lane; e < kGemvRS * R; e += 32) {
@@ -219,6 +234,58 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
         cp_async_arrive_noinc(&full[s]);
     }
     cp_async_wait_all();
+}
+
+// Few columns: four k of a consumer thread's A row (from the stage's
+// swizzled A tile) and the stage's four B rows of R columns.
+template <int R>
+struct GemvChunk {
+    float4 a;
+    float b[4][R];
+};
+
+template <int R>
+__device__ __forceinline__ void gemv_load_chunk(GemvChunk<R> &ch, const float *big, const float *small,
+                                                int c, int t) {
+    ch.a = reinterpret_cast<const float4 *>(big + t * kGemvRS)[c ^ (t & 7)];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float *brow = small + (4 * c + q) * R;
+        if constexpr (R >= 4) {
+#pragma unroll
+            for (int u = 0; u < R / 4; ++u) {
+                const float4 v = reinterpret_cast<const float4 *>(brow)[u];
+                ch.b[q][4 * u] = v.x;
+                ch.b[q][4 * u + 1] = v.y;
+                ch.b[q][4 * u + 2] = v.z;
+                ch.b[q][4 * u + 3] = v.w;
+            }
+        } else if constexpr (R == 2) {
+            const float2 v = reinterpret_cast<const float2 *>(brow)[0];
+            ch.b[q][0] = v.x;
+            ch.b[q][1] = v.y;
+        } else {
+            ch.b[q][0] = brow[0];
+        }
+    }
+}
+
+// The chunk's four terms, in increasing k, for each of the R outputs.
+template <int MODE, int R>
+__device__ __forceinline__ void gemv_run_chunk(const GemvChunk<R> &ch, float2 (&acc)[(R + 1) / 2],
+                                               float &acc1) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float a = q == 0 ? ch.a.x : q == 1 ? ch.a.y : q == 2 ? ch.a.z : ch.a.w;
+        if constexpr (R == 1) {
+            acc1 = term<MODE>(acc1, a, ch.b[q][0]);
+        } else {
+            const float2 a2 = make_float2(a, a);
+#pragma unroll
+            for (int h = 0; h < R / 2; ++h)
+                acc[h] = term2<MODE>(acc[h], a2, make_float2(ch.b[q][2 * h], ch.b[q][2 * h + 1]));
+        }
+    }
 }
 
 // C (m x n) = A (m x k) . B (k x n) with m <= R (ROWS: a block owns 32
@@ -254,17 +321,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     float acc1 = 0.0f;
 #pragma unroll
     for (int h = 0; h < (R + 1) / 2; ++h) acc[h] = make_float2(0.0f, 0.0f);
+    if constexpr (ROWS) {
 #pragma unroll 1
-    for (int kt = 0; kt < nk; ++kt) {
-        const int s = kt % kGemvStages;
-        if (!mbar_wait(&full[s], (kt / kGemvStages) & 1)) {
-            gemv_record_timeout();
-            return;
-        }
-        const float *big = reinterpret_cast<const float *>(base + s * kBigBytes);
-        const float *small = reinterpret_cast<const float *>(base + Sm::kSmallOff + s * Sm::kSmallBytes);
-        if constexpr (ROWS) {
-            const float *bcol = big + t;
+        for (int kt = 0; kt < nk; ++kt) {
+            const int s = kt % kGemvStages;
+            if (!mbar_wait(&full[s], (kt / kGemvStages) & 1)) {
+                gemv_record_timeout();
+                return;
+            }
+            const float *bcol = reinterpret_cast<const float *>(base + s * kBigBytes) + t;
+            const float *small = reinterpret_cast<const float *>(base + Sm::kSmallOff + s * Sm::kSmallBytes);
 #pragma unroll
             for (int r = 0; r < kGemvRS; ++r) {
                 const float b = bcol[r * kGemvOut];
@@ -277,28 +343,48 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                         acc[h] = term2<MODE>(acc[h], reinterpret_cast<const float2 *>(small + r * R)[h], b2);
                 }
             }
-        } else {
-            const float4 *arow = reinterpret_cast<const float4 *>(big + t * kGemvRS);
-#pragma unroll
-            for (int c = 0; c < kGemvRS / 4; ++c) {
-                const float4 a4 = arow[c ^ (t & 7)];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float a = q == 0 ? a4.x : q == 1 ? a4.y : q == 2 ? a4.z : a4.w;
-                    const float *brow = small + (4 * c + q) * R;
-                    if constexpr (R == 1) {
-                        acc1 = term<MODE>(acc1, a, brow[0]);
-                    } else {
-                        const float2 a2 = make_float2(a, a);
-#pragma unroll
-                        for (int h = 0; h < R / 2; ++h)
-                            acc[h] = term2<MODE>(acc[h], a2, reinterpret_cast<const float2 *>(brow)[h]);
-                    }
-                }
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+    } else {
+        // The thread's row runs in chunks of four k. Each chunk's operands are
+        // loaded while the previous chunk computes, and the next stage's first
+        // chunk while this stage's last one does, so shared-memory latency
+        // stays off the accumulators' dependency chain.
+        constexpr int kChunks = kGemvRS / 4;
+        auto big_of = [&](int s) { return reinterpret_cast<const float *>(base + s * kBigBytes); };
+        auto small_of = [&](int s) {
+            return reinterpret_cast<const float *>(base + Sm::kSmallOff + s * Sm::kSmallBytes);
+        };
+        if (!mbar_wait(&full[0], 0)) {
+            gemv_record_timeout();
+            return;
+        }
+        GemvChunk<R> cur, nxt;
+        gemv_load_chunk<R>(cur, big_of(0), small_of(0), 0, t);
+#pragma unroll 1
+        for (int kt = 0; kt < nk; ++kt) {
+            const int s = kt % kGemvStages;
+            const float *big = big_of(s), *small = small_of(s);
+#pragma unroll
+            for (int c = 0; c < kChunks - 1; ++c) {
+                gemv_load_chunk<R>(nxt, big, small, c + 1, t);
+                gemv_run_chunk<MODE, R>(cur, acc, acc1);
+                cur = nxt;
+            }
+            if (kt + 1 < nk) {
+                const int s1 = (kt + 1) % kGemvStages;
+                if (!mbar_wait(&full[s1], ((kt + 1) / kGemvStages) & 1)) {
+                    gemv_record_timeout();
+                    return;
+                }
+                gemv_load_chunk<R>(nxt, big_of(s1), small_of(s1), 0, t);
+            }
+            gemv_run_chunk<MODE, R>(cur, acc, acc1);
+            cur = nxt;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
     }
 
     const GemvBlock bl = gemv_block(g);
@@ -503,7 +589,6 @@ cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cud
         g.dH = static_cast<int>(p.dH); g.dW = static_cast<int>(p.dW);
         g.HW = HW;
         // ceil(2^32 / d): exact quotients for numerators below 2^24 and d <= 64
-        g.magic_taps = taps > 1 ? static_cast<uint32_t>(((uint64_t{1} << 32) + taps - 1) / taps) : 0u;
         g.magic_kw = p.KW > 1 ? static_cast<uint32_t>(((uint64_t{1} << 32) + p.KW - 1) / p.KW) : 0u;
     }
     return launch_gemv(g, mode, false, p.G, p.Cout, p.w_ld, s);
