@@ -146,6 +146,14 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
         step_c = kGemvRS / g.taps;
         step_t = kGemvRS - step_c * g.taps;
     }
+    // few columns, B read in place: the offset of this lane's column
+    // j = cg * R + lane % R, split into (row, column) of its index
+    int64_t col_off = 0;
+    if (!ROWS && !g.im2col) {
+        const int64_t j = static_cast<int64_t>(bl.cg) * R + lane % R;
+        const int64_t jy = j / g.b_jw, jx = j - jy * g.b_jw;
+        col_off = jy * g.b_sjy + jx * g.b_sj;
+    }
     const uint32_t base32 = smem_u32(base);
     for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % kGemvStages;
@@ -213,23 +221,24 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
                 tap_t -= g.taps;
                 ++tap_c;
             }
-        } else
-        for (int e = lane; e < kGemvRS * R; e += 32) {
-            const int r = e / R, q = e % R;
-            const int64_t p = p0 + r;
-            bool ok;
-            const float *src;
-            if constexpr (ROWS) {
-                ok = p < g.k && q < g.m;
-                src = ok ? A + q * g.a_si + p * g.a_sp : A;
-            } else {
-                ok = p < g.k && q < n_here;
-                // column j = cg * R + q of B, split into (row, column) of its index
-                const int64_t j = static_cast<int64_t>(bl.cg) * R + q;
-                const int64_t jy = j / g.b_jw, jx = j - jy * g.b_jw;
-                src = ok ? Bg + p * g.b_sp + jy * g.b_sjy + jx * g.b_sj : Bg;
+        } else {
+            // lane copies column q = lane % R of rows lane / R + (32 / R) i
+            const int q = lane % R;
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int r = lane / R + (kGemvRS / R) * i;
+                const int64_t p = p0 + r;
+                bool ok;
+                const float *src;
+                if constexpr (ROWS) {
+                    ok = p < g.k && q < g.m;
+                    src = ok ? A + q * g.a_si + p * g.a_sp : A;
+                } else {
+                    ok = p < g.k && q < n_here;
+                    src = ok ? Bg + p * g.b_sp + col_off : Bg;
+                }
+                cp_async_4_if(small32 + (r * R + q) * 4, src, ok);
             }
-            cp_async_4_if(small32 + e * 4, src, ok);
         }
         cp_async_arrive_noinc(&full[s]);
     }
@@ -562,9 +571,11 @@ cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cud
     auto blocks = [&](int w) { return (M + kGemvOut - 1) / kGemvOut * ((P + w - 1) / w) * p.N * p.G; };
     while (width > 2 && blocks(width) < num_sms()) width /= 2;
     // when choosing: gathered patches pay off with a long k loop and a block
-    // for every SM (measured on ResNet-50 at batch 1: the 7x7 stem ran faster
-    // in the few-pixel kernel)
+    // for every SM, and in-place columns with k of 128 or more (measured on
+    // ResNet-50 at batch 1: the 7x7 stem and the 64-channel 1x1 layers at
+    // 56 x 56 ran faster in the few-pixel kernel)
     if (choose && !direct && (p.K < 256 || blocks(width) < num_sms())) return cudaErrorNotSupported;
+    if (choose && direct && p.K < 128) return cudaErrorNotSupported;
     GemvProblem g{};
     g.m = M; g.n = P; g.k = p.K;
     g.A = p.w; g.a_si = p.w_ld; g.a_sp = 1;
