@@ -33,11 +33,27 @@ __device__ unsigned g_status_gemv;
 namespace {
 
 constexpr int kGemvOut = 32;      // outputs (columns or rows) per block, one per consumer thread
-constexpr int kGemvRS = 32;       // k per stage
-constexpr int kGemvStages = 12;   // ring depth
+// k per stage (tuning knob, a multiple of 32): a stage's fixed costs --
+// barrier waits and arrivals, copy issue -- are paid once per this many
+// terms on both the producer and the consumer side.
+#ifndef OM_GEMV_STAGE_K
+#define OM_GEMV_STAGE_K 64
+#endif
+constexpr int kGemvRS = OM_GEMV_STAGE_K;
+constexpr int kGemvBox = 32;                    // k per 128-byte-swizzled box of A
+constexpr int kGemvStages = 12 * 32 / kGemvRS;  // ring depth: 384 k in flight
+static_assert(kGemvRS % kGemvBox == 0 && kGemvRS <= 256, "whole boxes per stage");
 constexpr int kGemvThreads = kGemvOut + 32;  // consumers, then one producer warp
 constexpr int kGemvConsumerWarps = kGemvOut / 32;
 constexpr uint32_t kBigBytes = kGemvOut * kGemvRS * 4;  // large-operand tile of a stage
+
+// Few columns: float index of A element (row r, k kk) in a stage's A tile --
+// boxes of 32 k side by side, each [32 rows][32 k] with the 128-byte
+// swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)).
+__host__ __device__ constexpr int gemv_a_index(int r, int kk) {
+    return (kk / kGemvBox) * kGemvOut * kGemvBox + r * kGemvBox +
+           ((((kk % kGemvBox) >> 2) ^ (r & 7)) << 2) + (kk & 3);
+}
 
 // Shared memory: the large operand's stages (1 KB aligned, as the 128-byte
 // swizzle wants), the small operand's stages, then the full and empty
@@ -127,10 +143,10 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
     const float *B = g.B + grp * g.grp_b;
     const float *Bg = B + bl.img * g.img_b;  // this block's image
     const int64_t n_here = ROWS ? g.n : min(static_cast<int64_t>(R), g.n - static_cast<int64_t>(bl.cg) * R);
-    // im2col: lane r copies row r of every stage (tap p = kt * 32 + r) for
-    // all R columns. Per column, the input coordinates of its tap (0, 0);
-    // per lane, its tap's channel c and position t = ky * KW + kx in the
-    // kernel, advanced by 32 taps a stage.
+    // im2col: lane r copies rows r + 32h of every stage (taps
+    // p = kt * kGemvRS + r + 32h) for all R columns. Per column, the input
+    // coordinates of its tap (0, 0); per lane, its next tap's channel c and
+    // position t = ky * KW + kx in the kernel, advanced by 32 taps a row.
     int col_iy0[R], col_ix0[R];
     int tap_c = 0, tap_t = 0, step_c = 0, step_t = 0;
     if (!ROWS && g.im2col) {
@@ -143,8 +159,8 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
         }
         tap_c = lane / g.taps;
         tap_t = lane - tap_c * g.taps;
-        step_c = kGemvRS / g.taps;
-        step_t = kGemvRS - step_c * g.taps;
+        step_c = 32 / g.taps;
+        step_t = 32 - step_c * g.taps;
     }
     // few columns, B read in place: the offset of this lane's column
     // j = cg * R + lane % R, split into (row, column) of its index
@@ -179,8 +195,10 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
                 if constexpr (ROWS)
                     tma_load_2d(big, map, &full[s], static_cast<int>(o0), static_cast<int>(p0));
                 else
-                    tma_load_2d(big, map, &full[s], static_cast<int>(p0),
-                                static_cast<int>(grp * g.grp_map_rows + o0));
+                    for (int b = 0; b < kGemvRS / kGemvBox; ++b)
+                        tma_load_2d(big + b * kGemvOut * kGemvBox * 4, map, &full[s],
+                                    static_cast<int>(p0) + b * kGemvBox,
+                                    static_cast<int>(grp * g.grp_map_rows + o0));
             }
         } else if constexpr (ROWS) {
             // B rows of the stage, [32][32]
@@ -191,42 +209,46 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
                 cp_async_4_if(big32 + e * 4, ok ? B + p * g.b_sp + j * g.b_sj : B, ok);
             }
         } else {
-            // A rows of the block, [32][32], 16-byte chunk c of row r at c ^ (r % 8)
+            // A rows of the block, laid out as the TMA boxes would be
             for (int e = lane; e < kGemvOut * kGemvRS; e += 32) {
                 const int r = e / kGemvRS, kk = e % kGemvRS;
                 const int64_t i = o0 + r, p = p0 + kk;
                 const bool ok = i < g.m && p < g.k;
-                const uint32_t off = (r * kGemvRS + ((((kk >> 2) ^ (r & 7)) << 2) | (kk & 3))) * 4;
+                const uint32_t off = static_cast<uint32_t>(gemv_a_index(r, kk)) * 4;
                 cp_async_4_if(big32 + off, ok ? A + i * g.a_si + p * g.a_sp : A, ok);
             }
         }
         // the small operand: A columns [32][R] (few rows) or B rows [32][R] (few columns)
         if (!ROWS && g.im2col) {
-            const bool p_ok = p0 + lane < g.k;
-            const int ky = g.KW == 1 ? tap_t
-                                     : static_cast<int>(__umulhi(static_cast<uint32_t>(tap_t), g.magic_kw));
-            const int dy = ky * g.dH, dx = (tap_t - ky * g.KW) * g.dW;
-            const float *plane = Bg + (p_ok ? static_cast<int64_t>(tap_c) * g.HW : 0);
 #pragma unroll
-            for (int q = 0; q < R; ++q) {
-                const int iy = col_iy0[q] + dy, ix = col_ix0[q] + dx;
-                const bool ok = p_ok && q < n_here && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
-                                static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
-                const float *src = ok ? plane + (static_cast<int64_t>(iy) * g.W + ix) : Bg;
-                cp_async_4_if(small32 + (lane * R + q) * 4, src, ok);
-            }
-            tap_c += step_c;
-            tap_t += step_t;
-            if (tap_t >= g.taps) {
-                tap_t -= g.taps;
-                ++tap_c;
+            for (int h = 0; h < kGemvRS / 32; ++h) {
+                const int r = lane + 32 * h;
+                const bool p_ok = p0 + r < g.k;
+                const int ky = g.KW == 1 ? tap_t
+                                         : static_cast<int>(__umulhi(static_cast<uint32_t>(tap_t), g.magic_kw));
+                const int dy = ky * g.dH, dx = (tap_t - ky * g.KW) * g.dW;
+                const float *plane = Bg + (p_ok ? static_cast<int64_t>(tap_c) * g.HW : 0);
+#pragma unroll
+                for (int q = 0; q < R; ++q) {
+                    const int iy = col_iy0[q] + dy, ix = col_ix0[q] + dx;
+                    const bool ok = p_ok && q < n_here && static_cast<unsigned>(iy) < static_cast<unsigned>(g.H) &&
+                                    static_cast<unsigned>(ix) < static_cast<unsigned>(g.W);
+                    const float *src = ok ? plane + (static_cast<int64_t>(iy) * g.W + ix) : Bg;
+                    cp_async_4_if(small32 + (r * R + q) * 4, src, ok);
+                }
+                tap_c += step_c;
+                tap_t += step_t;
+                if (tap_t >= g.taps) {
+                    tap_t -= g.taps;
+                    ++tap_c;
+                }
             }
         } else {
             // lane copies column q = lane % R of rows lane / R + (32 / R) i
             const int q = lane % R;
 #pragma unroll
-            for (int i = 0; i < R; ++i) {
-                const int r = lane / R + (kGemvRS / R) * i;
+            for (int i = 0; i < R * kGemvRS / 32; ++i) {
+                const int r = lane / R + (32 / R) * i;
                 const int64_t p = p0 + r;
                 bool ok;
                 const float *src;
@@ -256,7 +278,7 @@ struct GemvChunk {
 template <int R>
 __device__ __forceinline__ void gemv_load_chunk(GemvChunk<R> &ch, const float *big, const float *small,
                                                 int c, int t) {
-    ch.a = reinterpret_cast<const float4 *>(big + t * kGemvRS)[c ^ (t & 7)];
+    ch.a = *reinterpret_cast<const float4 *>(big + gemv_a_index(t, 4 * c));
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float *brow = small + (4 * c + q) * R;
@@ -300,7 +322,8 @@ __device__ __forceinline__ void gemv_run_chunk(const GemvChunk<R> &ch, float2 (&
 // C (m x n) = A (m x k) . B (k x n) with m <= R (ROWS: a block owns 32
 // columns) or n <= R (!ROWS: a block owns 32 rows of group blockIdx.y).
 // TMA: the large operand comes by a 2-D tensor map (ROWS: B, box 32 columns
-// x 32 rows; !ROWS: A, box 32 k x 32 rows with the 128-byte swizzle).
+// x kGemvRS rows; !ROWS: A, boxes of 32 k x 32 rows with the 128-byte
+// swizzle, kGemvRS / 32 of them a stage).
 template <int MODE, int R, bool ROWS, bool TMA>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap map, const GemvProblem g) {
@@ -507,7 +530,7 @@ cudaError_t launch_gemv(GemvProblem g, int mode, bool rows, int64_t groups, int6
         tma = g.b_sj == 1 && gemv_map(&map, g.B, g.k, g.n, g.b_sp, kGemvOut, kGemvRS, false);
     else
         tma = g.a_sp == 1 && map_rows <= 0x7FFFFFFF - kGemvOut &&
-              gemv_map(&map, g.A, map_rows, g.k, map_ld, kGemvRS, kGemvOut, true);
+              gemv_map(&map, g.A, map_rows, g.k, map_ld, kGemvBox, kGemvOut, true);
     const int r = round_up_pow2(small);
     return mode == kFast ? launch_mode<kFast>(map, g, rows, tma, r, blocks, groups, s)
                          : launch_mode<kExact>(map, g, rows, tma, r, blocks, groups, s);
