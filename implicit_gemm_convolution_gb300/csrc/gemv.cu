@@ -201,7 +201,7 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
                                     static_cast<int>(grp * g.grp_map_rows + o0));
             }
         } else if constexpr (ROWS) {
-            // B rows of the stage, [32][32]
+            // B rows of the stage, [kGemvRS][32]
             for (int e = lane; e < kGemvRS * kGemvOut; e += 32) {
                 const int r = e / kGemvOut, c = e % kGemvOut;
                 const int64_t p = p0 + r, j = o0 + c;
