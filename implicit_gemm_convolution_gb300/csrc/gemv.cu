@@ -589,10 +589,13 @@ cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cud
                     P > (int64_t{1} << 30)))
         return cudaErrorNotSupported;
     if (P < 1) return cudaSuccess;
-    // columns per block: 8, or fewer while that leaves SMs without a block
+    // columns per block: 8, halved while there are fewer than two blocks per
+    // SM (measured on ResNet-50 at batch 1: fewer outputs per consumer warp
+    // beat the extra weight re-reads from L2 down to two blocks per SM, not to
+    // four)
     int width = kGemvMaxSmall;
     auto blocks = [&](int w) { return (M + kGemvOut - 1) / kGemvOut * ((P + w - 1) / w) * p.N * p.G; };
-    while (width > 2 && blocks(width) < num_sms()) width /= 2;
+    while (width > 1 && blocks(width) < 2 * static_cast<int64_t>(num_sms())) width /= 2;
     // when choosing: gathered patches pay off with a long k loop and a block
     // for every SM, and in-place columns with k of 128 or more (measured on
     // ResNet-50 at batch 1: the 7x7 stem and the 64-channel 1x1 layers at
