@@ -203,6 +203,37 @@ def time_calls(fn, steps: int, warmup: int, flush, stream) -> list[float]:
     return times
 
 
+def time_reps(fn, flush, stream, min_ms: float = 80.0, reps: int = 3, warmup: int = 3,
+              min_calls: int = 5) -> dict:
+    """The repetition method of the pages' benchmark applied on the device:
+    after warm-up calls, each repetition runs calls (L2 flushed before each,
+    CUDA events around each on the launching stream) until their summed device
+    time reaches min_ms; a repetition's figure is its mean per-call time, and
+    the result is the median over the repetitions."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    means, calls = [], []
+    for _ in range(reps):
+        total, count = 0.0, 0
+        while total < min_ms or count < min_calls:
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+            count += 1
+        means.append(total / count)
+        calls.append(count)
+    return {"ms": float(np.median(means)), "rep_ms": [round(v, 5) for v in means],
+            "calls_per_rep": calls}
+
+
 def combine_ranks(ms_local: float, flops_per_rank: float, world: int, dist=None, device="cpu"):
     """Replicas only: every rank ran the same workload on its own GPU with no
     exchange. Returns (the slowest rank's ms per step, whole-job GFLOP/s =
@@ -276,6 +307,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clocks.__exit__(None, None, None)
     ms_local = float(np.mean(kernel_ms))
     ms, value = combine_ranks(ms_local, flops, world, dist, dev)
+    reps = time_reps(step_exact, flush, stream, args.rep_ms)
     if dist is not None:
         dist.barrier()
     achieved_tflops = flops / (ms_local * 1e-3) / 1e12
@@ -370,12 +402,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                              workspace=wsp if use_ws else None)
             if st != 0:
                 raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
-        t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
+        r = time_reps(f, flush, stream, args.rep_ms)
+        t = r["ms"]
         fl = 2.0 * case_.m * case_.n * case_.k
         tf = fl / (t * 1e-3) / 1e12
         pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
         extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
-                        "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
+                        "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2),
+                        "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"]}
         if hbm_bound:
             extras[name].update(hbm_fields(4.0 * (case_.m * case_.k + case_.k * case_.n +
                                                   case_.m * case_.n), t))
@@ -398,7 +432,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                              case_.ldb, Cd.data_ptr(), case_.ldc, "tf32x3", stream)
             if st != 0:
                 raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
-        t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
+        r = time_reps(f, flush, stream, args.rep_ms)
+        t = r["ms"]
         fl = 2.0 * case_.m * case_.n * case_.k
         tf = fl / (t * 1e-3) / 1e12
         peaks = measured_peaks()
@@ -408,7 +443,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "tensor_frac": round(3 * tf / tf32_peak, 4),
                         "tensor_peak_tflops": round(tf32_peak, 1),
                         "tensor_peak_basis": peaks["basis"] + " x nominal tf32/bf16 ratio 1.1/2.25; "
-                                             "three tensor-core products per useful flop"}
+                                             "three tensor-core products per useful flop",
+                        "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"]}
 
     def conv_line(name, mode, c, use_ws=False, hbm_bound=False):
         x = torch.from_numpy(c.x).to(dev)
@@ -428,12 +464,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 st = L.om_conv2d_f32(*args, stream.cuda_stream)
             if st != 0:
                 raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
-        t = float(np.median(time_calls(f, args.extra_steps, 3, flush, stream)))
+        r = time_reps(f, flush, stream, args.rep_ms)
+        t = r["ms"]
         fl = 2.0 * c.N * c.Cout * OH * OW * (c.Cin // c.G) * c.KH * c.KW
         tf = fl / (t * 1e-3) / 1e12
         pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
         extras[name] = {"ms": round(t, 4), "GFLOP/s": round(tf * 1e3, 1),
-                        "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2)}
+                        "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2),
+                        "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"]}
         if hbm_bound:
             extras[name].update(hbm_fields(4.0 * (c.x.size + c.w.size + c.N * c.Cout * OH * OW), t))
 
@@ -444,8 +482,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         from implicit_gemm_convolution_gb300 import chain
         ch = chain.ConvChain(chain.resnet50_convs(), 1, 224, mode, device=dev)
         graph = ch.capture()
-        t_graph = float(np.median(time_calls(graph.replay, args.extra_steps, 3, flush, stream)))
-        t_eager = float(np.median(time_calls(ch.run, args.extra_steps, 3, flush, stream)))
+        t_graph = time_reps(graph.replay, flush, stream, args.rep_ms)["ms"]
+        t_eager = time_reps(ch.run, flush, stream, args.rep_ms)["ms"]
         tf = ch.flops / (t_graph * 1e-3) / 1e12
         pk = fp32_peak_tflops(sms, exact=(mode == "exact"))
         extras[name] = {"ms": round(t_graph, 4), "ms_eager_host_calls": round(t_eager, 4),
@@ -464,6 +502,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   synth.workload_gemm_prefill(False), use_ws=True)
         gemm_line("gemm_prefill_509x11005x4096_exact_ws", "exact",
                   synth.workload_gemm_prefill(True), use_ws=True)
+        gemm_line("gemm_prefill_512x11008x4096_fast_ws", "fast",
+                  synth.workload_gemm_prefill(False), use_ws=True)
+        gemm_line("gemm_prefill_509x11005x4096_fast_ws", "fast",
+                  synth.workload_gemm_prefill(True), use_ws=True)
         for md in ("exact", "fast"):
             conv_line(f"conv3x3_n32_c64_56_{md}_ws", md, synth.workload_conv3x3(), use_ws=True)
             conv_line(f"conv1x1_n32_c256to64_56_{md}_ws", md, synth.workload_conv1x1(), use_ws=True)
@@ -471,6 +513,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                   use_ws=True)
         gemm_line("gemm_prefill_512x11008x4096_exact", "exact", synth.workload_gemm_prefill(False))
         gemm_line("gemm_prefill_509x11005x4096_exact", "exact", synth.workload_gemm_prefill(True))
+        gemm_line("gemm_prefill_512x11008x4096_fast", "fast", synth.workload_gemm_prefill(False))
+        gemm_line("gemm_prefill_509x11005x4096_fast", "fast", synth.workload_gemm_prefill(True))
         for md in ("exact", "fast"):
             conv_line(f"conv3x3_n32_c64_56_{md}", md, synth.workload_conv3x3())
             conv_line(f"conv1x1_n32_c256to64_56_{md}", md, synth.workload_conv1x1())
@@ -515,32 +559,135 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "gpu_launches": args.steps,
         "clocks": clock_summary,
         "wall_s_timed_region": round(t_wall, 3),
+        "repetitions": {"ms_median": round(reps["ms"], 4),
+                        "GFLOP/s": round(flops / (reps["ms"] * 1e-3) / 1e9, 1),
+                        "rep_ms": reps["rep_ms"], "calls_per_rep": reps["calls_per_rep"],
+                        "method": f"after the timed steps: 3 repetitions of calls totalling >= "
+                                  f"{args.rep_ms:.0f} ms of device time each (L2 flushed before "
+                                  "every call), median of the repetitions' mean call times"},
         "modes": extras,
     }
     return line
 
 
-def cpu_baseline(seconds: float) -> dict:
-    """The oracle as it stands on the host cores: exact mode on a growing
-    sample of whole rows of the 4096-cube product until ~seconds of work."""
+def _cpu_rate(run, flops: float, min_s: float, reps: int = 3, warmup: int = 2) -> dict:
+    """The pages' benchmark method on the host: warm-up calls, then
+    repetitions of back-to-back calls lasting at least min_s each; the
+    figure is the median of the repetitions' rates."""
+    for _ in range(warmup):
+        run()
+    rates = []
+    for _ in range(reps):
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                break
+        rates.append(flops * calls / el / 1e9)
+    return {"gflops": float(np.median(rates)), "rates": [round(r, 4) for r in rates]}
+
+
+def cpu_baseline_cases():
+    """(name, full-workload flops, {threads-kind: (sample runner factory, sample flops, text)})
+    for every benchmark configuration. Samples are whole output rows of a
+    product, or whole images / output channels of a convolution: every
+    output is independent, so a sample's rate stands for the workload's."""
+    from implicit_gemm_convolution_gb300 import synth
     import oracle
-    case = gemm_workload()
+
+    def gemm_rows(case, rows):
+        A = np.ascontiguousarray(case.A[:rows])
+        C = np.ascontiguousarray(case.C_init[:rows]).copy()
+
+        def mk(mode, threads):
+            return lambda: oracle.gemm_raw(rows, case.n, case.k, A, case.lda, case.B, case.ldb, C,
+                                           case.ldc, mode, threads)
+        return mk, 2.0 * rows * case.n * case.k
+
+    def conv_part(c, images, out_channels):
+        x = np.ascontiguousarray(c.x[:images])
+        w = np.ascontiguousarray(c.w[:out_channels])
+        OH = (c.H + 2 * c.pad - c.dil * (c.KH - 1) - 1) // c.stride + 1
+        OW = (c.W + 2 * c.pad - c.dil * (c.KW - 1) - 1) // c.stride + 1
+
+        def mk(mode, threads):
+            return lambda: oracle.conv2d(x, w, c.stride, c.pad, c.dil, c.G, mode, threads)
+        return mk, 2.0 * images * out_channels * OH * OW * (c.Cin // c.G) * c.KH * c.KW
+
+    def conv_full_flops(c):
+        OH = (c.H + 2 * c.pad - c.dil * (c.KH - 1) - 1) // c.stride + 1
+        OW = (c.W + 2 * c.pad - c.dil * (c.KW - 1) - 1) // c.stride + 1
+        return 2.0 * c.N * c.Cout * OH * OW * (c.Cin // c.G) * c.KH * c.KW
+
+    T = oracle.default_threads()
+    out = []
+    small = synth.workload_gemm_small_strided()
+    mk, fl = gemm_rows(small, small.m)
+    out.append(("gemm_67x53x300_strided", fl, {"1": (mk, fl, "whole product"),
+                                               "all": (mk, fl, "whole product")}))
+    for name, case in (("gemm_4096^3", synth.workload_gemm_4096()),
+                       ("gemm_prefill_512x11008x4096", synth.workload_gemm_prefill(False)),
+                       ("gemm_prefill_509x11005x4096", synth.workload_gemm_prefill(True))):
+        full = 2.0 * case.m * case.n * case.k
+        m1, f1 = gemm_rows(case, 1)
+        mT, fT = gemm_rows(case, T)
+        out.append((name, full, {"1": (m1, f1, f"1 of {case.m} rows"),
+                                 "all": (mT, fT, f"{T} of {case.m} rows")}))
+    c3 = synth.workload_conv3x3()
+    m1, f1 = conv_part(c3, 1, 8)
+    mT, fT = conv_part(c3, 1, c3.Cout)
+    out.append(("conv3x3_n32_c64_56", conv_full_flops(c3),
+                {"1": (m1, f1, "image 0, output channels 0-7"),
+                 "all": (mT, fT, "image 0, all 64 output channels")}))
+    c1 = synth.workload_conv1x1()
+    m1, f1 = conv_part(c1, 1, 16)
+    mT, fT = conv_part(c1, 1, c1.Cout)
+    out.append(("conv1x1_n32_c256to64_56", conv_full_flops(c1),
+                {"1": (m1, f1, "image 0, output channels 0-15"),
+                 "all": (mT, fT, "image 0, all 64 output channels")}))
+    cg = synth.workload_conv_grouped()
+    m1, f1 = conv_part(cg, 1, cg.Cout)
+    mT, fT = conv_part(cg, cg.N, cg.Cout)
+    out.append(("conv_g32_s2_d2_n16_c256_28", conv_full_flops(cg),
+                {"1": (m1, f1, "image 0 of 16"), "all": (mT, fT, "all 16 images")}))
+    return out
+
+
+def cpu_baseline(seconds: float) -> dict:
+    """The oracle as it stands on the host cores, for every benchmark
+    configuration in both bit-exact modes, on one thread and on all cores
+    (OpenMP over output rows / (image, channel) pairs). Each figure is the
+    median of three repetitions of at least max(80 ms, ``seconds``/150 s) of back-to-back
+    calls on a sample of the workload; samples smaller than the whole
+    workload are labelled extrapolated (the full workload's time is its flops
+    over the sample's rate). The headline figure (``value``) is the 4096-cube
+    product in exact mode on all cores."""
+    import oracle
+    oracle.build()
     threads = oracle.default_threads()
-    rows = threads
-    elapsed = 0.0
-    while True:
-        Cs = np.zeros((rows, case.n), np.float32)
-        t0 = time.perf_counter()
-        oracle.gemm_raw(rows, case.n, case.k, case.A[:rows].copy(), case.k, case.B, case.n, Cs,
-                        case.n, oracle.EXACT, threads)
-        elapsed = time.perf_counter() - t0
-        if elapsed >= seconds / 4 or rows >= case.m:
-            break
-        rows = min(case.m, rows * 4)
-    gflops = 2.0 * rows * case.n * case.k / elapsed / 1e9
-    return {"value": round(gflops, 3), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"exact mode, first {rows} of 4096 rows of the 4096^3 product "
-                      f"({elapsed:.2f} s, OpenMP over rows)"}
+    min_s = max(0.08, seconds / 150.0)
+    rows = []
+    t_start = time.perf_counter()
+    for name, full, kinds in cpu_baseline_cases():
+        for mode_name, mode in (("exact", oracle.EXACT), ("fast", oracle.FAST)):
+            for kind, nthreads in (("1", 1), ("all", threads)):
+                mk, fl, text = kinds[kind]
+                r = _cpu_rate(mk(mode, nthreads), fl, min_s)
+                rows.append({"workload": name, "mode": mode_name, "threads": nthreads,
+                             "GFLOP/s": round(r["gflops"], 4),
+                             "full_ms": round(full / (r["gflops"] * 1e9) * 1e3, 2),
+                             "extrapolated": fl < full, "sample": text,
+                             "rep_GFLOP/s": r["rates"]})
+    head = next(r for r in rows if r["workload"] == "gemm_4096^3" and r["mode"] == "exact"
+                and r["threads"] == threads)
+    return {"value": head["GFLOP/s"], "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"exact mode, {head['sample']} of the 4096^3 product, all {threads} cores; "
+                      "median of 3 repetitions of back-to-back calls "
+                      f"(>= {min_s * 1e3:.0f} ms each) after 2 warm-up calls",
+            "per_workload": rows,
+            "wall_s": round(time.perf_counter() - t_start, 2)}
 
 
 def run_reference(args, rank: int):
@@ -636,8 +783,10 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--extra-steps", type=int, default=5)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rep-ms", type=float, default=80.0,
+                    help="device time per repetition of the per-workload lines (median of 3)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="scales the host baseline repetition length (max(80 ms, seconds/150) per repetition)")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--profile", default=None,
                     help="workload:mode (gemm_4096^3, gemm_prefill, gemm_prefill_ragged, gemm_decode,"

@@ -55,3 +55,33 @@ def test_scaled_resnet_chain_eager_and_graph(mode, name):
     for key in want:
         assert_bits_equal(ch.buf[key].cpu().numpy(), want[key], f"graph {key}")
     assert om.device_status() == 0
+
+
+@pytest.mark.parametrize("mode,name", [(oracle.EXACT, "exact"), (oracle.FAST, "fast")])
+def test_full_resnet50_chain_224_batch1(mode, name):
+    """The benchmark's chain at full size (ResNet-50's 53 convolutions,
+    224 x 224, batch 1, the benchmark's seeded weights and inputs), eagerly
+    and from the CUDA graph the benchmark replays: every activation buffer,
+    the last one included, bit for bit against the oracle."""
+    import torch
+    layers = chain.resnet50_convs()
+    shapes = chain.buffer_shapes(layers, 1, 224)
+    params = chain.make_params(layers)
+    inputs = chain.make_inputs(shapes)
+    want = oracle_chain(layers, inputs, params, mode)
+    ch = chain.ConvChain(layers, 1, 224, name, params=params, inputs=inputs)
+    ch.run()
+    torch.cuda.synchronize()
+    for key in want:
+        assert_bits_equal(ch.buf[key].cpu().numpy(), want[key], f"eager {key}")
+    g = ch.capture()
+    for key in want:
+        if key not in inputs:
+            ch.buf[key].fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    for key in want:
+        assert_bits_equal(ch.buf[key].cpu().numpy(), want[key], f"graph {key}")
+    assert om.device_status() == 0
+    last = layers[-1].dst
+    assert np.isfinite(want[last]).all() and (want[last] > 0).any()

@@ -51,6 +51,12 @@ MUTANTS = {
         "        if (bias) v = v + bias[(o / plane) % channels];\n        if (res) v = v + res[o];",
         "        if (bias && res) v = v + (bias[(o / plane) % channels] + res[o]);\n        else if (bias) v = v + bias[(o / plane) % channels];\n        else if (res) v = v + res[o];"),
     "epilogue_relu_drops_nan": ("!(v > 0.0f) && !isnan(v)", "!(v > 0.0f)"),
+    "f64_mag_without_fabs": ("t = t + fabs(prod);", "t = t + prod;"),
+    "f64_gemm_dropped_last_term": (
+        "            for (int64_t p = 0; p < k; ++p) {\n                const double prod",
+        "            for (int64_t p = 0; p + 1 < k; ++p) {\n                const double prod"),
+    "f64_conv_wrong_group": ("v = x[((n * Cin + g * cin_g + c) * H + iy) * W + ix];\n                                }\n                                const double",
+                             "v = x[((n * Cin + c) * H + iy) * W + ix];\n                                }\n                                const double"),
 }
 
 
@@ -71,6 +77,10 @@ def _build(tmp_path, name, old, new):
     L.oracle_conv_out_dim.restype = i64
     L.oracle_epilogue_f32.argtypes = [i64, i64, i64, vp, vp, vp, ci]
     L.oracle_epilogue_f32.restype = None
+    L.oracle_gemm_f64.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, vp, i64, ci]
+    L.oracle_gemm_f64.restype = None
+    L.oracle_conv2d_f64.argtypes = [i64] * 16 + [vp, vp, vp, vp, ci]
+    L.oracle_conv2d_f64.restype = None
     return L
 
 
@@ -135,10 +145,49 @@ def _pins_pass(L) -> bool:
                               None if r is None else r.ctypes.data, pin["act"])
         if y.view(np.uint32).tolist() != pin["out_bits"]:
             return False
+    if not _f64_pins_pass(L):
+        return False
     for cs in c["out_dims"]["cases"]:
         if L.oracle_conv_out_dim(cs["size"], cs["k"], cs["stride"], cs["pad"], cs["pad"], cs["dil"]) != cs["out"]:
             return False
     return True
+
+
+def _f64_pins_pass(L) -> bool:
+    """The binary64 companions on small integers of both signs: exact sums."""
+    rng = np.random.default_rng(5)
+    A = rng.integers(-9, 10, (4, 7))
+    B = rng.integers(-9, 10, (7, 3))
+    Ab, Bb = _slack(A.astype(np.float32)), _slack(B.astype(np.float32))
+    ref = np.zeros(12 + 4096)
+    mag = np.zeros(12 + 4096)
+    L.oracle_gemm_f64(4, 3, 7, Ab.ctypes.data, 7, Bb.ctypes.data, 3, ref.ctypes.data,
+                      mag.ctypes.data, 3, 1)
+    if not (np.array_equal(ref[:12].reshape(4, 3), A @ B)
+            and np.array_equal(mag[:12].reshape(4, 3), np.abs(A) @ np.abs(B))):
+        return False
+    # grouped convolution, 2 images, 4 -> 4 channels in 2 groups, 3x3, pad 1
+    x = rng.integers(-4, 5, (2, 4, 5, 5))
+    w = rng.integers(-4, 5, (4, 2, 3, 3))
+    xp = np.zeros((2, 4, 7, 7), np.int64)
+    xp[:, :, 1:6, 1:6] = x
+    want = np.zeros((2, 4, 5, 5), np.int64)
+    want_mag = np.zeros((2, 4, 5, 5), np.int64)
+    for oc in range(4):
+        g = oc // 2
+        for c in range(2):
+            for ky in range(3):
+                for kx in range(3):
+                    win = xp[:, g * 2 + c, ky:ky + 5, kx:kx + 5]
+                    want[:, oc] += w[oc, c, ky, kx] * win
+                    want_mag[:, oc] += abs(w[oc, c, ky, kx]) * np.abs(win)
+    xb, wb = _slack(x.astype(np.float32)), _slack(w.astype(np.float32))
+    ref = np.zeros(200 + 4096)
+    mag = np.zeros(200 + 4096)
+    L.oracle_conv2d_f64(2, 4, 5, 5, 4, 2, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, xb.ctypes.data,
+                        wb.ctypes.data, ref.ctypes.data, mag.ctypes.data, 1)
+    return (np.array_equal(ref[:200].reshape(want.shape), want)
+            and np.array_equal(mag[:200].reshape(want.shape), want_mag))
 
 
 def test_unmutated_copy_passes(tmp_path):

@@ -333,6 +333,34 @@ def test_grouped_workload_nonfinite_weights_reach_outputs():
     assert nan[:, nan_w_oc].all()
 
 
+def test_f64_companions_are_exact_sums_on_small_integers():
+    """The binary64 companions behind every error bound: with small integers
+    of both signs each product and partial sum is exact in binary64, so ref
+    must equal the integer sum of a*b and mag the integer sum of |a*b|
+    (a missing absolute value, a dropped term or a transposed index fails)."""
+    rng = np.random.default_rng(19)
+    A = rng.integers(-9, 10, (6, 11))
+    B = rng.integers(-9, 10, (11, 5))
+    ref, mag = oracle.gemm_f64(A.astype(np.float32), B.astype(np.float32))
+    assert np.array_equal(ref, (A @ B).astype(np.float64))
+    assert np.array_equal(mag, (np.abs(A) @ np.abs(B)).astype(np.float64))
+    assert (mag > np.abs(ref)).any()  # cancellation present, so |.| matters
+    for (N, Cin, H, W, Cout, G, KH, KW, s, p, d) in CONV_SHAPES:
+        x = rng.integers(-4, 5, (N, Cin, H, W))
+        w = rng.integers(-4, 5, (Cout, Cin // G, KH, KW))
+        ref, mag = oracle.conv2d_f64(x.astype(np.float32), w.astype(np.float32), s, p, d, G)
+        cols, OH, OW = im2col(x.astype(np.float32), KH, KW, s, p, d, G)
+        cog = Cout // G
+        wm = w.reshape(G, cog, -1)
+        for n in range(N):
+            for g in range(G):
+                cg = cols[n, g].astype(np.int64)
+                want = (wm[g] @ cg).reshape(cog, OH, OW)
+                want_mag = (np.abs(wm[g]) @ np.abs(cg)).reshape(cog, OH, OW)
+                assert np.array_equal(ref[n, g * cog:(g + 1) * cog], want.astype(np.float64))
+                assert np.array_equal(mag[n, g * cog:(g + 1) * cog], want_mag.astype(np.float64))
+
+
 def test_conv_thread_count_does_not_change_bits():
     case = synth.make_conv("t", 3, 8, 10, 10, 8, 2, 3, 3, 1, 1, 1, seed=42)
     ys = [bits(oracle.conv2d(case.x, case.w, 1, 1, 1, 2, 0, t)).copy() for t in (1, 4)]
