@@ -142,6 +142,7 @@ KERNEL_SOURCES = {
     "conv_implicit_kernel": ("conv_implicit.cu", "simt_tile.cuh", "om_device.cuh", "om_internal.h",
                              "schedule_host.h"),
     "gemm_tf32x3_kernel": ("gemm_tf32x3.cu", "om_device.cuh", "om_internal.h"),
+    "conv_rows_kernel": ("conv_rows.cu", "om_device.cuh", "om_internal.h"),
     "gemv_kernel": ("gemv.cu", "om_device.cuh", "om_internal.h"),
 }
 

@@ -22,8 +22,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libom_gpu.so")
 
-SOURCES = ["om_api.cu", "simple_kernels.cu", "sgemm_tiled.cu", "conv_implicit.cu", "conv_direct.cu", "gemv.cu",
-           "gemm_tf32x3.cu", "gemm_no_alloc.cu", "selftest.cu"]
+SOURCES = ["om_api.cu", "simple_kernels.cu", "sgemm_tiled.cu", "conv_implicit.cu", "conv_rows.cu",
+           "conv_direct.cu", "gemv.cu", "gemm_tf32x3.cu", "gemm_no_alloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-fmad=false", "-Xptxas", "--fmad=false",
                      "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

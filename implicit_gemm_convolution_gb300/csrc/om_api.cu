@@ -175,12 +175,14 @@ int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     if (e == cudaErrorNotSupported &&
         (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM)))
         e = om::launch_conv_direct(p, mode, s);
+    if (e == cudaErrorNotSupported && (cfg == om::kConvRows || cfg < 0))
+        e = om::launch_conv_rows(p, mode, cfg < 0, s);
     if (e == cudaErrorNotSupported && (cfg == om::kConvColumns || (cfg < 0 && few_pixels(p))))
         e = om::launch_conv_columns(p, mode, cfg < 0, s);
     if (e == cudaErrorNotSupported && (cfg == om::kConvSkinny || (cfg < 0 && few_pixels(p))))
         e = om::launch_conv_skinny(p, mode, s);
     if (e == cudaErrorNotSupported && cfg != om::kConvDirect && cfg != om::kConvGemv &&
-        cfg != om::kConvSkinny && cfg != om::kConvColumns)
+        cfg != om::kConvSkinny && cfg != om::kConvColumns && cfg != om::kConvRows)
         e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
     return from_cuda(e);
@@ -434,13 +436,14 @@ int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout,
 
 int om_device_status(void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned a = 0, b = 0, c = 0, d = 0, e = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0, e = 0, f = 0;
     if (om::read_clear_status_gemm(&a, s) != cudaSuccess) return OM_ERR_CUDA;
+    if (om::read_clear_status_rows(&f, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_conv(&b, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_tc(&c, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_gemv(&d, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_selftest(&e, s) != cudaSuccess) return OM_ERR_CUDA;
-    return ((a | b | c | d | e) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
+    return ((a | b | c | d | e | f) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
 }
 
 int om_selftest_wait_timeout(int which, int limit_ms, void *stream) {

@@ -74,6 +74,7 @@ enum ConvCfg : int {
     kConvGemv = 3,      // 1x1 over a 1x1 input: matrix-vector kernel
     kConvSkinny = 4,    // few output pixels: one pixel per thread, channels streamed in chunks
     kConvColumns = 5,   // blocks of 32 channels x 8 pixels, weights by TMA, patches gathered
+    kConvRows = 6,      // stride 1: warps own output-row segments of 64 channels, windows by TMA
 };
 
 // The direct kernel serves groups of up to kConvDirectMaxM output channels
@@ -99,6 +100,15 @@ cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s);
 // choose: decline gathered layers with a short k loop or too few blocks.
 cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cudaStream_t s);
 cudaError_t read_clear_status_gemv(unsigned *out, cudaStream_t s);
+
+// Stride-1 convolutions (3x3 with padding 1 or 1x1 unpadded, any kernel
+// height up to 7) whose output rows split into 14-pixel segments and whose
+// groups have a multiple of 64 output channels: each warp owns four row
+// segments of 64 channels, input windows by 4-D TMA with zero fill, the
+// weight block resident in shared memory. choose: decline when the warp
+// tasks would fill less than 80 % of the last round.
+cudaError_t launch_conv_rows(const ConvProblem &p, int mode, bool choose, cudaStream_t s);
+cudaError_t read_clear_status_rows(unsigned *out, cudaStream_t s);
 
 // Failure-detection self-test (selftest.cu): a one-block kernel whose
 // bounded wait (0: mbarrier phase, 1: global flag) runs out after limit_ms.

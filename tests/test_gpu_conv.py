@@ -11,7 +11,8 @@ from tests.gpu_util import (assert_bits_equal, forced_config, guarded_output, gu
 pytestmark = pytest.mark.gpu
 
 MODES = [(oracle.EXACT, "exact"), (oracle.FAST, "fast")]
-CFGS = [0, 1, 2, 4, 5, None]  # naive, implicit GEMM, direct small-group, few-pixel, 1x1 columns, default
+# naive, implicit GEMM, direct small-group, few-pixel, 1x1 columns, row segments, default
+CFGS = [0, 1, 2, 4, 5, 6, None]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -103,6 +104,19 @@ SMALL = [
     (4, 9, 7, 7, 512, 1, 3, 3, 1, 1, 1),
     (1, 300, 7, 7, 64, 1, 3, 3, 1, 1, 1),
     (8, 40, 7, 7, 1024, 1, 1, 1, 1, 0, 1),
+    # the row-segment kernel's shapes (stride 1; 3x3 padding 1 or 1x1
+    # unpadded; 64-channel blocks; output rows of 14, 28, 56 and 112 pixels):
+    # a ragged last input-channel stage, two and four channel blocks, two
+    # groups, rows spanning 1, 2 and 4 per warp task (and a 3x1 kernel, which
+    # it declines)
+    (2, 16, 28, 28, 64, 1, 3, 3, 1, 1, 1),
+    (3, 37, 28, 28, 128, 1, 3, 3, 1, 1, 1),
+    (2, 24, 16, 56, 64, 1, 1, 1, 1, 0, 1),
+    (1, 16, 4, 112, 128, 2, 3, 3, 1, 1, 1),
+    (2, 8, 30, 28, 64, 1, 3, 1, 1, 0, 1),
+    (4, 20, 14, 14, 256, 1, 1, 1, 1, 0, 1),
+    (2, 72, 8, 56, 64, 1, 3, 3, 1, 1, 1),
+    (2, 37, 8, 56, 64, 1, 1, 1, 1, 0, 1),
 ]
 
 
@@ -132,6 +146,18 @@ def test_padding_taps_with_nonfinite_weights(mode, name):
     c.w[3, 0, 2, 2] = np.nan
     for cfg in CFGS:
         assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"nonfinite cfg={cfg}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_padding_taps_with_nonfinite_weights_row_kernel(mode, name):
+    # a shape the row-segment kernel takes: non-finite weights on taps that
+    # meet the zero border the window copy writes
+    c = synth.make_conv("t", 2, 8, 14, 28, 64, 1, 3, 3, 1, 1, 1, seed=18)
+    c.w[5, 2, 0, 0] = np.inf
+    c.w[17, 7, 2, 2] = np.nan
+    c.w[63, 0, 1, 0] = -np.inf
+    for cfg in (6, None):
+        assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"nonfinite rows cfg={cfg}")
 
 
 @pytest.mark.parametrize("mode,name", MODES)
