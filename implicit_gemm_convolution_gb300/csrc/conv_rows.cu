@@ -38,15 +38,6 @@
 #include "om_internal.h"
 #include "om_device.cuh"
 
-// Tuning knob: 1 pairs the outputs of 1x1 kernels diagonally (channel a at
-// pixel j with channel b at pixel j+1, and the other diagonal, from a
-// pair-swapped weight copy: no broadcast operand, more shared loads); 0 pairs
-// them by channel with the input value broadcast, like the larger kernels
-// (measured faster: 93 against 103 us on the 1x1 ResNet-50 stage-1 layer).
-#ifndef OM_ROWS_DIAG_1X1
-#define OM_ROWS_DIAG_1X1 0
-#endif
-
 namespace om {
 
 __device__ unsigned g_status_rows;
@@ -75,7 +66,6 @@ struct RowsGeom {
     int box_floats, box_stride;  // floats copied per stage, floats between stages
     int stages;
     int w_vec;     // weight rows 16-byte aligned: 16-byte loads
-    int wt_pitch;  // floats per transposed weight row: 64, or 128 with the pair-swapped copy
     Epilogue ep;
 };
 
@@ -86,15 +76,17 @@ struct RowsSmem {
     float *win;
     uint64_t *full;
     int *abort_flag;
+    int *rec;  // per warp: [0] first chunk of the current task, [1] chunks issued, [2] chunks awaited
 };
 
 __device__ __forceinline__ RowsSmem rows_smem(uint8_t *raw, const RowsGeom &g) {
     RowsSmem s;
     uint8_t *base = raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
     s.wT = reinterpret_cast<float *>(base);
-    s.win = s.wT + g.K * g.wt_pitch;
+    s.win = s.wT + g.K * kRowsMB;
     s.full = reinterpret_cast<uint64_t *>(s.win + kRowsWarps * g.stages * g.box_stride);
     s.abort_flag = reinterpret_cast<int *>(s.full + kRowsWarps * g.stages);
+    s.rec = s.abort_flag + 4;
     return s;
 }
 
@@ -183,9 +175,7 @@ __device__ __forceinline__ void store_slice(const RowsGeom &g, const float *stg,
 }
 
 // Weight block b (64 output channels of one group) into shared memory,
-// transposed to [tap][channel] at the positions wt_pos gives (with a row
-// pitch of 128 floats, followed by the same row with the two channels of
-// every pair swapped). Consecutive
+// transposed to [tap][channel] at the positions wt_pos gives. Consecutive
 // threads take consecutive channels, so a warp's stores of one tap row hit
 // distinct banks; with 16-byte aligned rows each thread loads four taps at
 // once, kLoadBatch loads in flight before their values are stored.
@@ -208,21 +198,11 @@ __device__ __noinline__ void load_weight_block(const RowsGeom &g, float *wT, int
             for (int u = 0; u < kLoadBatch; ++u) {
                 const int e = e0 + u * kRowsThreads;
                 if (e < items) {
-                    const int ch = e & (kRowsMB - 1);
-                    const int P = g.wt_pitch;
-                    float *d = wT + (4 * (e / kRowsMB)) * P + wt_pos(ch);
+                    float *d = wT + (4 * (e / kRowsMB)) * kRowsMB + wt_pos(e & (kRowsMB - 1));
                     d[0] = vals[u].x;
-                    d[P] = vals[u].y;
-                    d[2 * P] = vals[u].z;
-                    d[3 * P] = vals[u].w;
-                    if (P != kRowsMB) {
-                        // the same tap rows with the channels of each pair swapped
-                        float *sw = wT + (4 * (e / kRowsMB)) * P + kRowsMB + wt_pos(ch ^ 1);
-                        sw[0] = vals[u].x;
-                        sw[P] = vals[u].y;
-                        sw[2 * P] = vals[u].z;
-                        sw[3 * P] = vals[u].w;
-                    }
+                    d[kRowsMB] = vals[u].y;
+                    d[2 * kRowsMB] = vals[u].z;
+                    d[3 * kRowsMB] = vals[u].w;
                 }
             }
         }
@@ -230,9 +210,7 @@ __device__ __noinline__ void load_weight_block(const RowsGeom &g, float *wT, int
         const int count = kRowsMB * g.K;
         for (int e = threadIdx.x; e < count; e += kRowsThreads) {
             const int ch = e & (kRowsMB - 1), k = e / kRowsMB;
-            const float val = __ldg(wb + static_cast<int64_t>(ch) * g.w_ld + k);
-            wT[k * g.wt_pitch + wt_pos(ch)] = val;
-            if (g.wt_pitch != kRowsMB) wT[k * g.wt_pitch + kRowsMB + wt_pos(ch ^ 1)] = val;
+            wT[k * kRowsMB + wt_pos(ch)] = __ldg(wb + static_cast<int64_t>(ch) * g.w_ld + k);
         }
     }
 }
@@ -246,16 +224,17 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     const RowsSmem sm = rows_smem(smem_raw, g);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tr = lane >> 2, tc = lane & 3;
+    // Per-warp task bookkeeping lives in shared memory (sm.rec) or is
+    // recomputed from the launch indices where it is needed, so that the
+    // accumulators and the operands of the inner loop own the registers.
     const int gw = blockIdx.x * kRowsWarps + warp;
-    const int WT = gridDim.x * kRowsWarps;
-    const int cnt = gw < g.NQ ? (g.NQ - 1 - gw) / WT + 1 : 0;  // tasks per weight block
-    const int per_block = cnt * g.nch;
-    const int total = per_block * g.nblocks;  // this warp's chunk sequence
+    const int cnt = gw < g.NQ ? (g.NQ - 1 - gw) / (gridDim.x * kRowsWarps) + 1 : 0;  // tasks per block
+    volatile int *rec = sm.rec + 4 * warp;
     uint64_t *full = sm.full + warp * g.stages;
     float *ring = sm.win + warp * g.stages * g.box_stride;
 
     if (lane == 0) {
-        for (int s = 0; s < g.stages; ++s) mbar_init(&full[s], 1);
+        for (int st = 0; st < g.stages; ++st) mbar_init(&full[st], 1);
         if (warp == 0) *sm.abort_flag = 0;
         fence_mbar_init();
         if (warp == 0) prefetch_tensormap(&mapX);
@@ -263,22 +242,22 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     __syncthreads();
     // Start the window stream before the weights: the copies overlap the
     // weight transpose.
-    int issued = 0;
     if (lane == 0) {
+        const int total = cnt * g.nch * g.nblocks;
+        int issued = 0;
         for (; issued < g.stages && issued < total; ++issued)
-            issue_chunk<PAD>(g, &mapX, ring + issued * g.box_stride, &full[issued], issued, per_block,
-                             gw, WT);
+            issue_chunk<PAD>(g, &mapX, ring + issued * g.box_stride, &full[issued], issued, cnt * g.nch,
+                             gw, gridDim.x * kRowsWarps);
+        rec[1] = issued;
+        rec[2] = 0;
     }
+    __syncwarp();
 
     // The thread's input window in a stage: the box column of its first
     // tap, rounded down to an 8-byte boundary (POFF = the remainder).
     constexpr int POFF = (PAD + 4 * ((PAD + 3) / 4)) & 1;
     constexpr int NV = (kRowsTN + KS - 1 + POFF + 1) / 2 * 2;  // window values loaded per row
-    // 1x1 kernels pair outputs diagonally (no broadcast operand)
-    constexpr bool DIAG = KS == 1 && OM_ROWS_DIAG_1X1;
-    const int box_rows = g.BH;
 
-    int i = 0;
     bool aborted = false;
     for (int b = 0; b < g.nblocks; ++b) {
         // ---- weight block b, transposed into shared memory by every thread
@@ -288,15 +267,17 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         if (*reinterpret_cast<volatile int *>(sm.abort_flag)) aborted = true;
 
         for (int r = 0; r < cnt; ++r) {
-            const int t = gw + r * WT;
-            const int n = t / g.Q, q = t - n * g.Q;
-            const int seg = 4 * q + tc;
-            const int oy = seg / g.SR;
-            const int ox0 = (seg - oy * g.SR) * kRowsTN;
-            const int oyq = (4 * q) / g.SR;
-            // first window value: box column ox0 - PAD - x0, rounded down to even
-            const int wcol = ox0 - PAD - g.x0 - POFF;
-            const int row0 = oy - oyq;
+            int toff;  // this thread's window offset in a stage: row row0, column wcol
+            {
+                const int t = gw + r * gridDim.x * kRowsWarps;
+                const int n = t / g.Q, q = t - n * g.Q;
+                const int seg = 4 * q + tc;
+                const int oy = seg / g.SR;
+                const int ox0 = (seg - oy * g.SR) * kRowsTN;
+                toff = (oy - (4 * q) / g.SR) * g.BW + ox0 - PAD - g.x0 - POFF;
+            }
+            if (lane == 0) rec[0] = (b * cnt + r) * g.nch;
+            __syncwarp();
 
             float2 acc[4][kRowsTN];
 #pragma unroll
@@ -304,148 +285,117 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
 #pragma unroll
                 for (int j = 0; j < kRowsTN; ++j) acc[p][j] = make_float2(0.0f, 0.0f);
 
-            int s = 0;
-            for (int ch = 0; ch < g.nch; ++ch, ++i) {
-                s = i % g.stages;
-                const uint32_t parity = static_cast<uint32_t>((i / g.stages) & 1);
-                const float *stage = ring + s * g.box_stride;
-                if (!aborted) {
-                    if (!mbar_wait(&full[s], parity)) {
+            // One loop over the task's input channels (the accumulators stay
+            // in one loop nest); at each stage boundary the finished stage is
+            // handed back to the copy engine and the next one awaited.
+            int left = 0;                            // channels left in the stage
+            const float *cwin = ring;                // this thread's window rows of channel c
+            const float *wk = sm.wT + 4 * tr;        // weight rows of channel c's taps
+            for (int c = 0; c < g.cin_g && !aborted; ++c) {
+                if (left == 0) {
+                    const int ci = rec[0] + c / g.CC;  // chunk index of channel c
+                    if (c != 0) {
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int issued = rec[1];
+                            const int per_block = cnt * g.nch;
+                            if (issued < per_block * g.nblocks) {
+                                // every lane's reads of the finished stage are done
+                                // (syncwarp); order them before the async proxy
+                                // overwrites it
+                                const int sp = (ci - 1) % g.stages;
+                                fence_proxy_async_smem();
+                                issue_chunk<PAD>(g, &mapX, ring + sp * g.box_stride, &full[sp], issued,
+                                                 per_block, gw, gridDim.x * kRowsWarps);
+                                rec[1] = issued + 1;
+                            }
+                        }
+                    }
+                    const int sl = ci % g.stages;
+                    if (!mbar_wait(&full[sl], static_cast<uint32_t>((ci / g.stages) & 1))) {
                         rows_record_timeout(sm.abort_flag);
                         aborted = true;
+                        break;
                     }
+                    if (lane == 0) rec[2] = ci + 1;
+                    cwin = ring + sl * g.box_stride + toff;
+                    left = min(g.CC, g.cin_g - c);
                 }
-                if (!aborted) {
-                    const int cc_n = min(g.CC, g.cin_g - ch * g.CC);
-                    const float *wrow = stage + row0 * g.BW + wcol;
-                    if constexpr (DIAG) {
-                        // 1x1: acc[p][2jj] holds (channel 2p at pixel 2jj,
-                        // channel 2p+1 at pixel 2jj+1) and acc[p][2jj+1] the
-                        // other diagonal; both take the input pair
-                        // (pixel 2jj, 2jj+1), with the weight pair direct or
-                        // swapped -- every operand is a register pair as loaded.
-                        const float *wk = sm.wT + (ch * g.CC) * (2 * kRowsMB) + 4 * tr;
-#pragma unroll 2
-                        for (int c = 0; c < cc_n; ++c) {
-                            const float *wr0 = wrow + c * box_rows * g.BW;
-                            float2 bp[kRowsTN / 2];
+                --left;
+                if constexpr (KS == 1) {
+                    // 1x1: channel pairs with the input value broadcast
+                    float2 bp[kRowsTN / 2];
 #pragma unroll
-                            for (int u = 0; u < kRowsTN / 2; ++u) bp[u] = *reinterpret_cast<const float2 *>(wr0 + 2 * u);
-                            const float4 a0 = *reinterpret_cast<const float4 *>(wk);
-                            const float4 a1 = *reinterpret_cast<const float4 *>(wk + 32);
-                            const float4 s0 = *reinterpret_cast<const float4 *>(wk + 64);
-                            const float4 s1 = *reinterpret_cast<const float4 *>(wk + 96);
-                            const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
-                                                  make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
-                            const float2 sp[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
-                                                  make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
+                    for (int u = 0; u < kRowsTN / 2; ++u) bp[u] = *reinterpret_cast<const float2 *>(cwin + 2 * u);
+                    const float4 a0 = *reinterpret_cast<const float4 *>(wk);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(wk + 32);
+                    const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
+                                          make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
 #pragma unroll
-                            for (int u = 0; u < kRowsTN / 2; ++u) {
+                    for (int u = 0; u < kRowsTN / 2; ++u) {
+                        const float2 bx = make_float2(bp[u].x, bp[u].x);
+                        const float2 by = make_float2(bp[u].y, bp[u].y);
 #pragma unroll
-                                for (int p = 0; p < 4; ++p) {
-                                    acc[p][2 * u] = pterm<MODE>(acc[p][2 * u], ap[p], bp[u]);
-                                    acc[p][2 * u + 1] = pterm<MODE>(acc[p][2 * u + 1], sp[p], bp[u]);
-                                }
-                            }
-                            wk += 2 * kRowsMB;
+                        for (int p = 0; p < 4; ++p) {
+                            acc[p][2 * u] = pterm<MODE>(acc[p][2 * u], bx, ap[p]);
+                            acc[p][2 * u + 1] = pterm<MODE>(acc[p][2 * u + 1], by, ap[p]);
                         }
-                    } else if constexpr (KS == 1) {
-                        // 1x1, channel pairs with the input value broadcast; the
-                        // next channel's operands load while this channel's
-                        // terms run (software pipelining across the chunk)
-                        const float *wk = sm.wT + (ch * g.CC) * kRowsMB + 4 * tr;
-                        float2 vb[kRowsTN / 2];
-                        float4 a0, a1;
-#pragma unroll
-                        for (int u = 0; u < kRowsTN / 2; ++u) vb[u] = *reinterpret_cast<const float2 *>(wrow + 2 * u);
-                        a0 = *reinterpret_cast<const float4 *>(wk);
-                        a1 = *reinterpret_cast<const float4 *>(wk + 32);
+                    }
+                    wk += kRowsMB;
+                } else {
 #pragma unroll 1
-                        for (int c = 0; c < cc_n; ++c) {
-                            const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
-                                                  make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
-                            float v[kRowsTN];
+                    for (int ky = 0; ky < KS; ++ky) {
+                        // window row row0 + ky of channel c in the stage
+                        const float *wr0 = cwin + ky * g.BW;
+                        float v[NV];
 #pragma unroll
-                            for (int u = 0; u < kRowsTN / 2; ++u) {
-                                v[2 * u] = vb[u].x;
-                                v[2 * u + 1] = vb[u].y;
-                            }
-                            if (c + 1 < cc_n) {
-                                const float *wr1 = wrow + (c + 1) * box_rows * g.BW;
-#pragma unroll
-                                for (int u = 0; u < kRowsTN / 2; ++u) vb[u] = *reinterpret_cast<const float2 *>(wr1 + 2 * u);
-                                a0 = *reinterpret_cast<const float4 *>(wk + kRowsMB);
-                                a1 = *reinterpret_cast<const float4 *>(wk + kRowsMB + 32);
-                            }
-#pragma unroll
-                            for (int j = 0; j < kRowsTN; ++j) {
-                                const float2 b2 = make_float2(v[j], v[j]);
-#pragma unroll
-                                for (int p = 0; p < 4; ++p) acc[p][j] = pterm<MODE>(acc[p][j], b2, ap[p]);
-                            }
-                            wk += kRowsMB;
+                        for (int u = 0; u < NV / 2; ++u) {
+                            const float2 t2 = *reinterpret_cast<const float2 *>(wr0 + 2 * u);
+                            v[2 * u] = t2.x;
+                            v[2 * u + 1] = t2.y;
                         }
-                    } else {
-                    const float *wk = sm.wT + (ch * g.CC) * (KS * KS * kRowsMB) + 4 * tr;
-#pragma unroll 1
-                    for (int c = 0; c < cc_n; ++c) {
-#pragma unroll 1
-                        for (int ky = 0; ky < KS; ++ky) {
-                            // window row c * BH + row0 + ky of the stage
-                            const float *wr0 = wrow + (c * box_rows + ky) * g.BW;
-                            float v[NV];
+                        // the two channel pairs of each half of the thread's
+                        // eight channels, per kernel column
+                        float2 ap[KS][4];
 #pragma unroll
-                            for (int u = 0; u < NV / 2; ++u) {
-                                const float2 t2 = *reinterpret_cast<const float2 *>(wr0 + 2 * u);
-                                v[2 * u] = t2.x;
-                                v[2 * u + 1] = t2.y;
-                            }
-                            // the two channel pairs of each half of the thread's
-                            // eight channels, per kernel column
-                            float2 ap[KS][4];
+                        for (int kx = 0; kx < KS; ++kx) {
+                            const float *wr = wk + (ky * KS + kx) * kRowsMB;
+                            const float4 a0 = *reinterpret_cast<const float4 *>(wr);
+                            const float4 a1 = *reinterpret_cast<const float4 *>(wr + 32);
+                            ap[kx][0] = make_float2(a0.x, a0.y);
+                            ap[kx][1] = make_float2(a0.z, a0.w);
+                            ap[kx][2] = make_float2(a1.x, a1.y);
+                            ap[kx][3] = make_float2(a1.z, a1.w);
+                        }
+                        // per output the kernel columns go in order: output j
+                        // of column kx reads window value j + kx
+#pragma unroll
+                        for (int j = 0; j < kRowsTN; ++j) {
 #pragma unroll
                             for (int kx = 0; kx < KS; ++kx) {
-                                const float *wr = wk + (ky * KS + kx) * kRowsMB;
-                                const float4 a0 = *reinterpret_cast<const float4 *>(wr);
-                                const float4 a1 = *reinterpret_cast<const float4 *>(wr + 32);
-                                ap[kx][0] = make_float2(a0.x, a0.y);
-                                ap[kx][1] = make_float2(a0.z, a0.w);
-                                ap[kx][2] = make_float2(a1.x, a1.y);
-                                ap[kx][3] = make_float2(a1.z, a1.w);
-                            }
-                            // per output the kernel columns go in order:
-                            // output j of column kx reads window value j + kx
+                                const float bv = v[j + kx + POFF];
+                                const float2 b2 = make_float2(bv, bv);
 #pragma unroll
-                            for (int j = 0; j < kRowsTN; ++j) {
-#pragma unroll
-                                for (int kx = 0; kx < KS; ++kx) {
-                                    const float bv = v[j + kx + POFF];
-                                    const float2 b2 = make_float2(bv, bv);
-#pragma unroll
-                                    for (int p = 0; p < 4; ++p) acc[p][j] = pterm<MODE>(acc[p][j], b2, ap[kx][p]);
-                                }
+                                for (int p = 0; p < 4; ++p) acc[p][j] = pterm<MODE>(acc[p][j], b2, ap[kx][p]);
                             }
                         }
-                        wk += KS * KS * kRowsMB;
                     }
-                    }
+                    wk += KS * KS * kRowsMB;
                 }
-                __syncwarp();
-                if (ch != g.nch - 1 && !aborted && lane == 0 && issued < total) {
-                    // every lane's reads of this stage are done (syncwarp);
-                    // order them before the async proxy overwrites it
-                    fence_proxy_async_smem();
-                    issue_chunk<PAD>(g, &mapX, ring + s * g.box_stride, &full[s], issued, per_block,
-                                     gw, WT);
-                    ++issued;
-                }
+                cwin += g.BH * g.BW;
             }
+            __syncwarp();
+            if (aborted) continue;
             // ---- epilogue through the last stage (the next copy into it is
             // issued afterwards): per channel slot cs, the eight thread rows'
             // channels 8*tr + cs as eight rows of the warp's four segments,
             // then 8-byte stores along output rows.
             {
-                float *stg = ring + s * g.box_stride;
+                const int last = rec[0] + g.nch - 1;
+                const int sl = last % g.stages;
+                float *stg = ring + sl * g.box_stride;
+                const int t = gw + r * gridDim.x * kRowsWarps;
+                const int n = t / g.Q, q = t - n * g.Q;
                 const int grp = b / g.mblocks, mb = b - grp * g.mblocks;
                 const int ch_base = grp * g.M + mb * kRowsMB;
                 const int64_t ybase = static_cast<int64_t>(n) * g.Cout * g.OH * g.OW;
@@ -458,38 +408,35 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 }
 #pragma unroll
                 for (int cs = 0; cs < 8; ++cs) {
-                    if (!aborted) {
 #pragma unroll
-                        for (int j = 0; j < kRowsTN; j += 2) {
-                            float2 o;
-                            if constexpr (DIAG)
-                                o = (cs & 1) ? make_float2(acc[cs >> 1][j + 1].x, acc[cs >> 1][j].y)
-                                             : make_float2(acc[cs >> 1][j].x, acc[cs >> 1][j + 1].y);
-                            else
-                                o = (cs & 1) ? make_float2(acc[cs >> 1][j].y, acc[cs >> 1][j + 1].y)
-                                             : make_float2(acc[cs >> 1][j].x, acc[cs >> 1][j + 1].x);
-                            *reinterpret_cast<float2 *>(stg + tr * kRowsStagePitch + tc * kRowsTN + j) = o;
-                        }
+                    for (int j = 0; j < kRowsTN; j += 2) {
+                        const float2 o = (cs & 1) ? make_float2(acc[cs >> 1][j].y, acc[cs >> 1][j + 1].y)
+                                                  : make_float2(acc[cs >> 1][j].x, acc[cs >> 1][j + 1].x);
+                        *reinterpret_cast<float2 *>(stg + tr * kRowsStagePitch + tc * kRowsTN + j) = o;
                     }
                     __syncwarp();
-                    if (!aborted)
-                        store_slice<HAS_EP>(g, stg, lane, ybase, seg_off[0], seg_off[1], seg_off[2], seg_off[3],
-                                            ch_base + cs);
+                    store_slice<HAS_EP>(g, stg, lane, ybase, seg_off[0], seg_off[1], seg_off[2], seg_off[3],
+                                        ch_base + cs);
                     __syncwarp();
                 }
-                if (!aborted && lane == 0 && issued < total) {
-                    fence_proxy_async_smem();
-                    issue_chunk<PAD>(g, &mapX, ring + s * g.box_stride, &full[s], issued, per_block, gw,
-                                     WT);
-                    ++issued;
+                if (lane == 0) {
+                    const int issued = rec[1];
+                    const int per_block = cnt * g.nch;
+                    if (issued < per_block * g.nblocks) {
+                        fence_proxy_async_smem();
+                        issue_chunk<PAD>(g, &mapX, ring + sl * g.box_stride, &full[sl], issued, per_block, gw,
+                                         gridDim.x * kRowsWarps);
+                        rec[1] = issued + 1;
+                    }
                 }
             }
         }
     }
     // Copies still in flight (only after a timeout) must land before the
     // CTA's shared memory is released.
+    __syncwarp();
     if (lane == 0) {
-        for (int j = i; j < issued; ++j)
+        for (int j = rec[2]; j < rec[1]; ++j)
             (void)mbar_wait(&full[j % g.stages], static_cast<uint32_t>((j / g.stages) & 1));
     }
 }
@@ -601,7 +548,6 @@ cudaError_t launch_conv_rows(const ConvProblem &p, int mode, bool choose, cudaSt
     g.nblocks = static_cast<int>(p.G) * g.mblocks;
     const int KW = static_cast<int>(p.KW), PAD = static_cast<int>(p.pL);
     g.w_vec = (g.K % 4 == 0) && (g.w_ld % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.w) & 15) == 0);
-    g.wt_pitch = (KW == 1 && OM_ROWS_DIAG_1X1) ? 2 * kRowsMB : kRowsMB;
     const int RQ = g.SR >= 4 ? 1 : 4 / g.SR;  // output rows per task
     g.BH = RQ - 1 + g.KH;
     g.x0 = -4 * ((PAD + 3) / 4);
@@ -614,8 +560,8 @@ cudaError_t launch_conv_rows(const ConvProblem &p, int mode, bool choose, cudaSt
     // Stage size: as many input channels as fit with two or three stages per
     // warp beside the weight block (at most 32; a stage also holds the
     // epilogue's 8 x 60-float staging rows).
-    const int64_t wt_bytes = static_cast<int64_t>(g.K) * g.wt_pitch * 4;
-    const int64_t budget = static_cast<int64_t>(max_smem_optin()) - wt_bytes - 128 - 16 -
+    const int64_t wt_bytes = static_cast<int64_t>(g.K) * kRowsMB * 4;
+    const int64_t budget = static_cast<int64_t>(max_smem_optin()) - wt_bytes - 128 - 16 - kRowsWarps * 16 -
                            static_cast<int64_t>(kRowsWarps) * 3 * 8;
     const int64_t row_floats = static_cast<int64_t>(g.BW) * g.BH;
     int best_cc = 0, best_st = 0;
@@ -639,7 +585,7 @@ cudaError_t launch_conv_rows(const ConvProblem &p, int mode, bool choose, cudaSt
     g.box_floats = g.BW * g.BH * g.CC;
     g.box_stride = (g.box_floats + 31) / 32 * 32;
     const int64_t smem = wt_bytes + static_cast<int64_t>(kRowsWarps) * g.stages * g.box_stride * 4 +
-                         static_cast<int64_t>(kRowsWarps) * g.stages * 8 + 16 + 128;
+                         static_cast<int64_t>(kRowsWarps) * g.stages * 8 + 16 + kRowsWarps * 16 + 128;
     if (smem > max_smem_optin()) return cudaErrorNotSupported;
     const int64_t nwarps_needed = (static_cast<int64_t>(g.NQ) + 0);
     int64_t grid = (nwarps_needed + kRowsWarps - 1) / kRowsWarps;
