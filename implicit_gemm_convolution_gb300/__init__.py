@@ -85,6 +85,10 @@ def lib() -> ctypes.CDLL:
             L.om_device_status.restype = ci
             L.om_device_status.argtypes = [vp]
             L.om_selftest_wait_timeout.argtypes = [ci, ci, vp]
+            L.om_selftest_wait_timeout_ws.restype = ci
+            L.om_selftest_wait_timeout_ws.argtypes = [ci, ci, vp, ctypes.c_size_t, vp]
+            L.om_workspace_status.restype = ci
+            L.om_workspace_status.argtypes = [vp, ctypes.c_size_t, vp]
             L.om_workspace_bytes.restype = ctypes.c_size_t
             L.om_gemm_f32_ex.restype = ci
             L.om_gemm_f32_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp, i64, ci,
@@ -270,8 +274,15 @@ def conv2d_packed(x, w_packed, w_shape, stride: int = 1, padding: int = 0, dilat
 
 
 def device_status(stream=None) -> int:
-    """Synchronises the stream and returns (and clears) the device status word."""
+    """Synchronises the stream and returns (and clears) the device-wide status
+    words (timeouts of calls made without a workspace)."""
     return int(lib().om_device_status(_stream_handle(stream)))
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the status word of a
+    workspace: timeouts of the calls that were given this workspace."""
+    return int(lib().om_workspace_status(*_ws_args(workspace), _stream_handle(stream)))
 
 
 def _ptr_or_none(t):

@@ -53,10 +53,11 @@ struct ConvGeom {
     int K, w_ld;
     int tiles_m, tiles_n, G;
     Epilogue ep;
+    unsigned *status;  // the call's status word in a caller workspace, or NULL
 };
 
-__device__ __forceinline__ void conv_record_timeout(int *abort_flag) {
-    atomicOr(&g_status_conv, kDevErrTimeout);
+__device__ __forceinline__ void conv_record_timeout(unsigned *status, int *abort_flag) {
+    report_timeout(status, &g_status_conv);
     *reinterpret_cast<volatile int *>(abort_flag) = 1;
 }
 
@@ -162,7 +163,7 @@ __device__ __forceinline__ void conv_produce(const ConvGeom &g, const CUtensorMa
         }
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
-                conv_record_timeout(abort_flag);
+                conv_record_timeout(g.status, abort_flag);
                 cp_async_wait_all();
                 if (A_TMA && pt == 0) {
                     // let the weight tiles already requested land first
@@ -386,14 +387,14 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kConvProducers, 1)
         acc.zero();
         if (sg.kind == kSegLate) {
             if (!wait_previous_part(sched.flags, Cfg::CONSUMERS, abort_flag)) {
-                atomicOr(&g_status_conv, kDevErrTimeout);
+                report_timeout(g.status, &g_status_conv);
                 return;
             }
             conv_tile_io<Cfg, 2, false>(g, acc, tm, tn, grp, arow0, bcol0);
         }
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&full[stage], phase)) {
-                conv_record_timeout(abort_flag);
+                conv_record_timeout(g.status, abort_flag);
                 return;
             }
             const float *As = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE_BYTES);
@@ -462,6 +463,7 @@ static cudaError_t launch_conv_cfg(const ConvProblem &p, unsigned *flags, cudaSt
     g.K = static_cast<int>(p.K); g.w_ld = static_cast<int>(p.w_ld);
     g.G = static_cast<int>(p.G);
     g.ep = p.ep;
+    g.status = p.status;
     const int64_t tiles_m = (g.M + Cfg::BM - 1) / Cfg::BM;
     const int64_t tiles_n = (g.ncols + Cfg::BN - 1) / Cfg::BN;
     if (tiles_m * tiles_n * p.G > 0x7FFFFFFF || p.w_ld > 0x7FFFFFFF) return cudaErrorNotSupported;
@@ -502,8 +504,13 @@ static cudaError_t launch_conv_cfg(const ConvProblem &p, unsigned *flags, cudaSt
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                smem_bytes);
     if (e != cudaSuccess) return e;
-    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kConvProducers, smem_bytes, s, map, g,
-                            sched);
+    cudaError_t el = launch_scheduled(kernel, sched, Cfg::CONSUMERS + kConvProducers, smem_bytes, s, map, g,
+                                      sched);
+    if (el == cudaErrorCooperativeLaunchTooLarge) {
+        const Schedule whole = whole_tiles(sched);
+        el = launch_scheduled(kernel, whole, Cfg::CONSUMERS + kConvProducers, smem_bytes, s, map, g, whole);
+    }
+    return el;
 }
 
 cudaError_t launch_conv_implicit(const ConvProblem &p, int mode, int cfg, unsigned *flags,

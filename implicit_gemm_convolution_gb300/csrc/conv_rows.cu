@@ -67,6 +67,7 @@ struct RowsGeom {
     int stages;
     int w_vec;     // weight rows 16-byte aligned: 16-byte loads
     Epilogue ep;
+    unsigned *status;  // the call's status word in a caller workspace, or NULL
 };
 
 // Shared memory: the transposed weight block, kRowsWarps rings of window
@@ -110,8 +111,8 @@ __device__ __forceinline__ float2 pterm(float2 acc, float2 a, float2 b) {
     }
 }
 
-__device__ __forceinline__ void rows_record_timeout(int *abort_flag) {
-    atomicOr(&g_status_rows, kDevErrTimeout);
+__device__ __forceinline__ void rows_record_timeout(unsigned *status, int *abort_flag) {
+    report_timeout(status, &g_status_rows);
     *reinterpret_cast<volatile int *>(abort_flag) = 1;
 }
 
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                     }
                     const int sl = ci % g.stages;
                     if (!mbar_wait(&full[sl], static_cast<uint32_t>((ci / g.stages) & 1))) {
-                        rows_record_timeout(sm.abort_flag);
+                        rows_record_timeout(g.status, sm.abort_flag);
                         aborted = true;
                         break;
                     }
@@ -557,6 +558,7 @@ cudaError_t launch_conv_rows(const ConvProblem &p, int mode, bool choose, cudaSt
     g.BW = (max_col + 1 + 3) / 4 * 4;
     if (g.BW > 256 || g.BH > 256) return cudaErrorNotSupported;
     g.ep = p.ep;
+    g.status = p.status;
     // Stage size: as many input channels as fit with two or three stages per
     // warp beside the weight block (at most 32; a stage also holds the
     // epilogue's 8 x 60-float staging rows).

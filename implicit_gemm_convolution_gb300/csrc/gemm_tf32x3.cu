@@ -139,13 +139,15 @@ struct Bars {
     uint64_t drained;  // one commit after the last MMA: every MMA has finished
     uint32_t tmem_base;
     int abort;
+    unsigned *status;  // the call's status word in a caller workspace, or NULL
 };
+static_assert(sizeof(Bars) <= 256, "the barriers fit the 256 bytes reserved after the stages");
 
 __device__ __forceinline__ bool aborted(Bars *b) {
     return *reinterpret_cast<volatile int *>(&b->abort) != 0;
 }
 __device__ __forceinline__ void fail(Bars *b) {
-    atomicOr(&g_status_tc, kDevErrTimeout);
+    report_timeout(b->status, &g_status_tc);
     *reinterpret_cast<volatile int *>(&b->abort) = 1;
 }
 // Bounded wait that also gives up once another role has failed.
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         }
         mbar_init(&bars->drained, 1);
         bars->abort = 0;
+        bars->status = p.status;
         fence_mbar_init();
         fence_proxy_async_smem();
     }

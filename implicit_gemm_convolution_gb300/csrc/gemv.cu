@@ -98,6 +98,7 @@ struct GemvProblem {
     int H, W, OW, KW, taps, sH, sW, pT, pL, dH, dW;
     int64_t HW;
     uint32_t magic_kw;  // t / KW = umulhi(t, magic_kw) for t < taps
+    unsigned *status;   // the call's status word in a caller workspace, or NULL
 };
 
 struct GemvBlock {
@@ -125,7 +126,7 @@ __device__ __forceinline__ uint8_t *gemv_smem_base(uint8_t *raw) {
     return raw + ((1024u - (b & 1023u)) & 1023u);
 }
 
-__device__ __forceinline__ void gemv_record_timeout() { atomicOr(&g_status_gemv, kDevErrTimeout); }
+__device__ __forceinline__ void gemv_record_timeout(unsigned *status) { report_timeout(status, &g_status_gemv); }
 
 // Producer warp of both kernels. Stage kt: the large operand's tile by TMA
 // (lane 0, when TMA) or by 4-byte copies of every lane, and the small
@@ -174,7 +175,7 @@ __device__ __forceinline__ void gemv_produce(const GemvProblem &g, const CUtenso
     for (int kt = 0; kt < nk; ++kt) {
         const int s = kt % kGemvStages;
         if (!mbar_wait(&empty[s], ((kt / kGemvStages) & 1) ^ 1)) {
-            gemv_record_timeout();
+            gemv_record_timeout(g.status);
             cp_async_wait_all();
             if (TMA && lane == 0) {
                 // let the tiles already requested land before leaving
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         for (int kt = 0; kt < nk; ++kt) {
             const int s = kt % kGemvStages;
             if (!mbar_wait(&full[s], (kt / kGemvStages) & 1)) {
-                gemv_record_timeout();
+                gemv_record_timeout(g.status);
                 return;
             }
             const float *bcol = reinterpret_cast<const float *>(base + s * kBigBytes) + t;
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             return reinterpret_cast<const float *>(base + Sm::kSmallOff + s * Sm::kSmallBytes);
         };
         if (!mbar_wait(&full[0], 0)) {
-            gemv_record_timeout();
+            gemv_record_timeout(g.status);
             return;
         }
         GemvChunk<R> cur, nxt;
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             if (kt + 1 < nk) {
                 const int s1 = (kt + 1) % kGemvStages;
                 if (!mbar_wait(&full[s1], ((kt + 1) / kGemvStages) & 1)) {
-                    gemv_record_timeout();
+                    gemv_record_timeout(g.status);
                     return;
                 }
                 gemv_load_chunk<R>(nxt, big_of(s1), small_of(s1), 0, t);
@@ -547,6 +548,7 @@ cudaError_t launch_gemm_gemv(const GemmProblem &p, int mode, cudaStream_t s) {
     g.bias = p.ep.bias; g.bias_si = 0; g.bias_sj = 1;
     g.res = p.ep.res; g.res_si = p.ep.ldr; g.res_sj = 1;
     g.act = p.ep.act;
+    g.status = p.status;
     if (p.m <= kGemvMaxSmall) return launch_gemv(g, mode, true, 1, 0, 0, s);
     if (p.n <= kGemvMaxSmall) return launch_gemv(g, mode, false, 1, p.m, p.lda, s);
     return cudaErrorNotSupported;
@@ -568,6 +570,7 @@ cudaError_t launch_conv_gemv(const ConvProblem &p, int mode, cudaStream_t s) {
     g.bias = p.ep.bias; g.bias_si = 1; g.bias_sj = 0;
     g.res = p.ep.res; g.res_si = 1; g.res_sj = p.Cout;
     g.act = p.ep.act;
+    g.status = p.status;
     g.grp_a = M * p.w_ld; g.grp_b = cin_g; g.grp_c = M; g.grp_bias = M; g.grp_res = M;
     g.grp_map_rows = M;
     return launch_gemv(g, mode, false, p.G, p.Cout, p.w_ld, s);
@@ -611,6 +614,7 @@ cudaError_t launch_conv_columns(const ConvProblem &p, int mode, bool choose, cud
     g.bias = p.ep.bias; g.bias_si = 1; g.bias_sj = 0;
     g.res = p.ep.res; g.res_si = P; g.res_sj = 1;
     g.act = p.ep.act;
+    g.status = p.status;
     g.grp_a = M * p.w_ld; g.grp_b = cin_g * HW; g.grp_c = M * P; g.grp_bias = M; g.grp_res = M * P;
     g.grp_map_rows = M;
     g.col_width = width;

@@ -193,16 +193,20 @@ int check_workspace(void *ws, size_t bytes, unsigned **flags) {
     *flags = nullptr;
     if (!ws) return OM_OK;
     if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return OM_ERR_ALIGNMENT;
-    if (bytes < static_cast<size_t>(om::kMaxScheduleCtas) * sizeof(unsigned)) return OM_ERR_INVALID_ARG;
+    if (bytes < static_cast<size_t>(om::kWorkspaceWords) * sizeof(unsigned)) return OM_ERR_INVALID_ARG;
     *flags = static_cast<unsigned *>(ws);
     return OM_OK;
 }
 
-Range ws_range(const unsigned *flags) { return span(flags, flags ? om::kMaxScheduleCtas : 0); }
+Range ws_range(const unsigned *flags) { return span(flags, flags ? om::kWorkspaceWords : 0); }
+
+// The status word of the calls that use a workspace, or NULL without one
+// (kernels then report into their translation unit's device-wide word).
+unsigned *ws_status(unsigned *flags) { return flags ? flags + om::kWsStatusWord : nullptr; }
 
 int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, const float *B,
               int64_t ldb, float *C, int64_t ldc, int mode, void *workspace, size_t ws_bytes,
-              void *stream, const om::Epilogue &ep = om::Epilogue{}) {
+              void *stream, const om::Epilogue &ep = om::Epilogue{}, bool status_in_ws = true) {
     if (m < 0 || n < 0 || k < 0) return OM_ERR_INVALID_ARG;
     if (mode != OM_MODE_EXACT && mode != OM_MODE_FAST && mode != OM_MODE_TF32X3)
         return OM_ERR_UNSUPPORTED;
@@ -238,7 +242,7 @@ int gemm_impl(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, cons
         if (overlaps(rres, rc) || (flags && overlaps(rres, rw))) return OM_ERR_ALIAS;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc, ep};
+    GemmProblem p{m, n, k, A, lda, B, ldb, C, ldc, ep, status_in_ws ? ws_status(flags) : nullptr};
     if (mode == OM_MODE_TF32X3) {
         if (k == 0) return from_cuda(om::launch_gemm_naive(p, OM_MODE_EXACT, s));  // +0
         cudaError_t e = om::launch_gemm_tf32x3(p, s);
@@ -298,6 +302,7 @@ int conv_impl(const ConvArgs &a, const float *x, const float *w, bool packed, fl
         if (overlaps(rr, ry) || (flags && overlaps(rr, rw))) return OM_ERR_ALIAS;
     }
     p.ep = ep;
+    p.status = ws_status(flags);
     return run_conv(p, mode, flags, static_cast<cudaStream_t>(stream));
 }
 
@@ -310,7 +315,10 @@ namespace om {
 int gemm_with_scratch(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda,
                       const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
                       void *scratch, size_t scratch_bytes, void *stream) {
-    return gemm_impl(m, n, k, A, lda, B, ldb, C, ldc, mode, scratch, scratch_bytes, stream);
+    // the library's own scratch has no reader for a status word: timeouts go
+    // to the device-wide words that om_device_status reads
+    return gemm_impl(m, n, k, A, lda, B, ldb, C, ldc, mode, scratch, scratch_bytes, stream,
+                     om::Epilogue{}, false);
 }
 
 }  // namespace om
@@ -343,7 +351,7 @@ int64_t om_conv_out_dim(int64_t size, int64_t ksize, int64_t stride, int64_t pad
 }
 
 size_t om_workspace_bytes(void) {
-    return static_cast<size_t>(om::kMaxScheduleCtas) * sizeof(unsigned);
+    return static_cast<size_t>(om::kWorkspaceWords) * sizeof(unsigned);
 }
 
 int om_gemm_f32(int64_t m, int64_t n, int64_t k, const float *A, int64_t lda, const float *B,
@@ -448,7 +456,34 @@ int om_device_status(void *stream) {
 
 int om_selftest_wait_timeout(int which, int limit_ms, void *stream) {
     if ((which != 0 && which != 1) || limit_ms < 1 || limit_ms > 1000) return OM_ERR_INVALID_ARG;
-    return from_cuda(om::launch_wait_timeout(which, limit_ms, static_cast<cudaStream_t>(stream)));
+    return from_cuda(om::launch_wait_timeout(which, limit_ms, nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+int om_selftest_wait_timeout_ws(int which, int limit_ms, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    if ((which != 0 && which != 1) || limit_ms < 1 || limit_ms > 1000) return OM_ERR_INVALID_ARG;
+    if (!workspace) return OM_ERR_NULL_PTR;
+    unsigned *flags = nullptr;
+    const int wst = check_workspace(workspace, workspace_bytes, &flags);
+    if (wst != OM_OK) return wst;
+    return from_cuda(om::launch_wait_timeout(which, limit_ms, ws_status(flags), static_cast<cudaStream_t>(stream)));
+}
+
+int om_workspace_status(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace) return OM_ERR_NULL_PTR;
+    unsigned *flags = nullptr;
+    const int wst = check_workspace(workspace, workspace_bytes, &flags);
+    if (wst != OM_OK) return wst;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, ws_status(flags), sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return OM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return OM_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemsetAsync(ws_status(flags), 0, sizeof(unsigned), s) != cudaSuccess) return OM_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return OM_ERR_CUDA;
+    }
+    return (word & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
 }
 
 }  // extern "C"

@@ -22,6 +22,13 @@ enum Mode : int { kExact = 0, kFast = 1 };
 // ran out; om_device_status() reads and clears the words.
 constexpr unsigned kDevErrTimeout = 1u;
 
+// Records a bounded wait that ran out: into the calling entry point's own
+// status word when it has one (a word of the caller's workspace), else into
+// the translation unit's device-wide word.
+__device__ __forceinline__ void report_timeout(unsigned *call_status, unsigned *tu_word) {
+    atomicOr(call_status != nullptr ? call_status : tu_word, kDevErrTimeout);
+}
+
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
 

@@ -29,6 +29,7 @@ struct GemmProblem {
     float *C;
     int64_t ldc;
     Epilogue ep;
+    unsigned *status;  // the call's status word in a caller workspace, or NULL
 };
 
 // A validated convolution problem. Weights are read as the matrix
@@ -44,6 +45,7 @@ struct ConvProblem {
     const float *w;
     float *y;
     Epilogue ep;
+    unsigned *status;  // the call's status word in a caller workspace, or NULL
 };
 
 // Kernel configurations the dispatcher can choose. A test-only environment
@@ -112,7 +114,7 @@ cudaError_t read_clear_status_rows(unsigned *out, cudaStream_t s);
 
 // Failure-detection self-test (selftest.cu): a one-block kernel whose
 // bounded wait (0: mbarrier phase, 1: global flag) runs out after limit_ms.
-cudaError_t launch_wait_timeout(int which, int limit_ms, cudaStream_t s);
+cudaError_t launch_wait_timeout(int which, int limit_ms, unsigned *status, cudaStream_t s);
 cudaError_t read_clear_status_selftest(unsigned *out, cudaStream_t s);
 
 cudaError_t launch_gemm_naive(const GemmProblem &p, int mode, cudaStream_t s);
@@ -149,8 +151,13 @@ cudaError_t read_clear_status_conv(unsigned *out, cudaStream_t s);
 int max_smem_optin();
 int num_sms();
 
-// Largest grid the balanced schedule runs (one flag word per CTA).
-constexpr int kMaxScheduleCtas = 1024;
+// Caller workspace of the *_ws / *_ex entry points: kWorkspaceWords 32-bit
+// words; words [0, kMaxScheduleCtas) are the balanced schedule's flags (one
+// per CTA), word kWsStatusWord the status word of the calls that use the
+// workspace.
+constexpr int kWorkspaceWords = 1024;
+constexpr int kMaxScheduleCtas = 1023;
+constexpr int kWsStatusWord = 1023;
 
 // Bit of the device status words set by a bounded wait that ran out.
 constexpr unsigned kDevErrTimeoutHost = 1u;

@@ -46,7 +46,22 @@ cudaError_t launch_scheduled(Kernel kernel, const Schedule &sched, int threads, 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+    const cudaError_t el = cudaLaunchKernelEx(&cfg, kernel, args...);
+    // Fewer SMs than the device has can be available to this context (MPS
+    // limits, partitioned contexts): the cooperative launch is then refused.
+    // The caller reruns the problem with the whole-tile schedule, which gives
+    // the same bits and needs no co-residency.
+    if (el == cudaErrorCooperativeLaunchTooLarge) (void)cudaGetLastError();
+    return el;
+}
+
+// Whole tiles only: the schedule to fall back to when a balanced launch is
+// refused for lack of co-resident CTAs.
+inline Schedule whole_tiles(const Schedule &balanced) {
+    Schedule s = balanced;
+    s.dp_tiles = s.tiles;
+    s.flags = nullptr;
+    return s;
 }
 
 }  // namespace om

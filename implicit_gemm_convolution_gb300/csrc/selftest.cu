@@ -1,6 +1,7 @@
 // Failure-detection self-test: makes one of the library's bounded device
 // waits run out on purpose, so that a test can check that the timeout is
-// reported through om_device_status and that the context stays usable.
+// reported (through the caller's workspace status word, or om_device_status
+// without a workspace) and that the context stays usable.
 //
 // The waits are the kernels' own: an mbarrier phase wait (the TMA / cp.async
 // pipelines) and a flag acquire (the balanced schedule's k-block
@@ -22,7 +23,7 @@ __device__ unsigned g_flag_never_set;  // zero-initialised, never written
 
 namespace {
 
-__global__ void wait_timeout_kernel(int which, unsigned long long limit_ns) {
+__global__ void wait_timeout_kernel(int which, unsigned long long limit_ns, unsigned *status) {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);  // one arrival completes phase 0; none comes
@@ -32,13 +33,14 @@ __global__ void wait_timeout_kernel(int which, unsigned long long limit_ns) {
     if (threadIdx.x != 0) return;
     const bool ok = which == 0 ? mbar_wait_limit(&bar, 0, limit_ns)
                                : acquire_flag(&g_flag_never_set, limit_ns);
-    if (!ok) atomicOr(&g_status_selftest, kDevErrTimeout);
+    if (!ok) report_timeout(status, &g_status_selftest);
 }
 
 }  // namespace
 
-cudaError_t launch_wait_timeout(int which, int limit_ms, cudaStream_t s) {
-    wait_timeout_kernel<<<1, 32, 0, s>>>(which, static_cast<unsigned long long>(limit_ms) * 1000000ull);
+cudaError_t launch_wait_timeout(int which, int limit_ms, unsigned *status, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>(which, static_cast<unsigned long long>(limit_ms) * 1000000ull,
+                                         status);
     return cudaGetLastError();
 }
 

@@ -40,8 +40,8 @@ __device__ unsigned g_status_gemm;
 // kProdMixed: A by TMA, B by 4-byte cp.async (B rows not 16-byte aligned).
 enum Producer : int { kProdTma = 0, kProdAsync = 1, kProdMixed = 2 };
 
-__device__ __forceinline__ void record_timeout(int *abort_flag) {
-    atomicOr(&g_status_gemm, kDevErrTimeout);
+__device__ __forceinline__ void record_timeout(unsigned *status, int *abort_flag) {
+    report_timeout(status, &g_status_gemm);
     *reinterpret_cast<volatile int *>(abort_flag) = 1;
 }
 
@@ -50,7 +50,7 @@ template <class Cfg>
 __device__ __forceinline__ void produce_tma(const CUtensorMap *mapA, const CUtensorMap *mapB,
                                             uint8_t *smem, uint64_t *full, uint64_t *empty,
                                             int *abort_flag, const TileRaster &rs,
-                                            const Schedule &sched) {
+                                            const Schedule &sched, unsigned *status) {
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -61,7 +61,7 @@ __device__ __forceinline__ void produce_tma(const CUtensorMap *mapA, const CUten
         rs.at(sg.tile, tm, tn);
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
-                record_timeout(abort_flag);
+                record_timeout(status, abort_flag);
                 // Let the copies already issued land before shared memory goes away.
                 for (int s = 0; s < Cfg::STAGES; ++s) {
                     if (issued > s) {
@@ -105,7 +105,7 @@ __device__ __forceinline__ void produce_async(const GemmProblem &p, uint8_t *sme
         const int64_t m0 = static_cast<int64_t>(tm) * BM, n0 = static_cast<int64_t>(tn) * BN;
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
-                record_timeout(abort_flag);
+                record_timeout(p.status, abort_flag);
                 cp_async_wait_all();
                 return;
             }
@@ -160,7 +160,7 @@ __device__ __forceinline__ void produce_mixed(const GemmProblem &p, const CUtens
         const int64_t n0 = static_cast<int64_t>(tn) * BN;
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
-                record_timeout(abort_flag);
+                record_timeout(p.status, abort_flag);
                 cp_async_wait_all();
                 if (pt == 0) {
                     // let the A tiles already requested land first
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
             if (warp == Cfg::CONSUMER_WARPS && lane == 0) {
                 prefetch_tensormap(&mapA);
                 prefetch_tensormap(&mapB);
-                produce_tma<Cfg>(&mapA, &mapB, smem, full, empty, abort_flag, rs, sched);
+                produce_tma<Cfg>(&mapA, &mapB, smem, full, empty, abort_flag, rs, sched, p.status);
             }
         } else if constexpr (PROD == kProdMixed) {
             if (threadIdx.x == Cfg::CONSUMERS) prefetch_tensormap(&mapA);
@@ -321,14 +321,14 @@ __global__ void __launch_bounds__(Cfg::CONSUMERS + kProducerThreads, 1)
         acc.zero();
         if (sg.kind == kSegLate) {
             if (!wait_previous_part(sched.flags, Cfg::CONSUMERS, abort_flag)) {
-                atomicOr(&g_status_gemm, kDevErrTimeout);
+                report_timeout(p.status, &g_status_gemm);
                 return;
             }
             tile_io<Cfg, 2>(p, acc, row0, col0, vec_store);
         }
         for (int kt = sg.kb; kt < sg.ke; ++kt) {
             if (!mbar_wait(&full[stage], phase)) {
-                record_timeout(abort_flag);
+                record_timeout(p.status, abort_flag);
                 return;
             }
             const float *As = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE_BYTES);
@@ -425,8 +425,14 @@ static cudaError_t launch_cfg(const GemmProblem &p, unsigned *flags, cudaStream_
     make_schedule(static_cast<int>(tm * tn), static_cast<int>((p.k + Cfg::BK - 1) / Cfg::BK),
                   flags, &sched);
     const int vec = ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) && (p.ldc % 4 == 0);
-    return launch_scheduled(kernel, sched, Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s,
-                            mapA, mapB, p, rs, sched, vec);
+    cudaError_t el = launch_scheduled(kernel, sched, Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s,
+                                      mapA, mapB, p, rs, sched, vec);
+    if (el == cudaErrorCooperativeLaunchTooLarge) {
+        const Schedule whole = whole_tiles(sched);
+        el = launch_scheduled(kernel, whole, Cfg::CONSUMERS + kProducerThreads, Cfg::SMEM_BYTES, s, mapA,
+                              mapB, p, rs, whole, vec);
+    }
+    return el;
 }
 
 using Cfg128x256 = TileCfg<128, 256, 8, 16, 2, 4, 4, true>;

@@ -65,7 +65,7 @@ typedef enum om_status {
     OM_ERR_ALIAS = 3,       /* the output range overlaps an input range */
     OM_ERR_UNSUPPORTED = 4, /* unknown mode, or a mode with no kernel for this call (reported, never approximated) */
     OM_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
-    OM_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up (see om_device_status) */
+    OM_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up (om_device_status, om_workspace_status) */
     OM_ERR_ALIGNMENT = 7,   /* a pointer is not 4-byte aligned, or packed weights not 16-byte aligned */
     OM_ERR_TOO_LARGE = 8    /* a size exceeds what the kernels index (see each entry point) */
 } om_status;
@@ -129,10 +129,29 @@ OM_API int om_gemm_f32(int64_t m, int64_t n, int64_t k,
                        int mode, void *stream);
 
 /*
- * Bytes of device scratch the *_ws entry points need (a constant: one 32-bit
- * flag per CTA of the balanced schedule, for grids of up to 1024 CTAs).
+ * Bytes of device scratch the *_ws and *_ex entry points take (a constant,
+ * 4096): 1024 32-bit words; words 0..1022 hold one flag per CTA of the
+ * balanced schedule (grids of up to 1023 CTAs), word 1023 is the status word
+ * of the calls that use the workspace. A bounded device wait that runs out in
+ * such a call records OM_ERR_TIMEOUT in that word -- not in the device-wide
+ * words of om_device_status -- so every caller with its own workspace sees
+ * only its own calls' timeouts (om_workspace_status). Zero a new workspace
+ * once before its first use; afterwards the library keeps the flags and
+ * om_workspace_status clears the status word.
  */
 OM_API size_t om_workspace_bytes(void);
+
+/*
+ * Synchronises stream, then reads and clears the status word of workspace
+ * (the word every *_ws / *_ex call given this workspace, and
+ * om_selftest_wait_timeout_ws, reports a timed-out device wait in). Returns
+ * OM_OK, OM_ERR_TIMEOUT if one of those calls' kernels gave up a bounded
+ * wait (its outputs are then incomplete), OM_ERR_NULL_PTR / OM_ERR_INVALID_ARG
+ * / OM_ERR_ALIGNMENT for a missing, short or misaligned workspace, or
+ * OM_ERR_CUDA if the copy or the synchronisation failed. The pages have no
+ * counterpart: this is the library's per-call failure report.
+ */
+OM_API int om_workspace_status(void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * om_gemm_f32 with caller scratch for a balanced schedule. Output tiles are
@@ -174,9 +193,10 @@ OM_API int om_gemm_f32_ws(int64_t m, int64_t n, int64_t k,
  * (1024 words, one per SM used) that every GPU loading the library holds
  * until the process exits. OM_ERR_TOO_LARGE if the device has more than 1024
  * SMs.
- * The first call on a device looks up that array's device address with the
- * device current (cudaGetSymbolAddress); make that first call before any
- * stream capture. No call allocates or frees device memory.
+ * The first call on a device (and the first call after the device's
+ * context changed, e.g. after cudaDeviceReset) looks up that array's device
+ * address with the device current (cudaGetSymbolAddress); make that first
+ * call before any stream capture. No call allocates or frees device memory.
  * All calls share the one array and it keeps the previous call's contents;
  * each call clears the words it needs on its stream before its kernel runs.
  * Calls that may overlap on the GPU (other streams, other threads) race on
@@ -310,12 +330,17 @@ OM_API int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W,
                             void *stream);
 
 /*
- * Synchronises stream, then reads and clears the library's device status
+ * Synchronises stream, then reads and clears the library's device-wide status
  * words for the current device. Every device-side wait in the library's
  * kernels (mbarrier waits of the TMA and tensor-core pipelines) is bounded;
- * a wait that runs out records OM_ERR_TIMEOUT there and the kernel returns
- * early instead of hanging. Returns OM_OK, OM_ERR_TIMEOUT, or OM_ERR_CUDA if
- * the synchronisation itself failed.
+ * a wait that runs out records OM_ERR_TIMEOUT and the kernel returns early
+ * instead of hanging. Calls given a workspace record it in the workspace's
+ * status word (om_workspace_status); calls without one (om_gemm_f32,
+ * om_conv2d_f32, om_conv2d_f32_packed, om_gemm_f32_no_alloc, the *_ex entry
+ * points with a NULL workspace) record it in these device-wide words, which
+ * every such call on the device shares: whichever caller reads them first
+ * sees (and clears) any such timeout. Returns OM_OK, OM_ERR_TIMEOUT, or
+ * OM_ERR_CUDA if the synchronisation itself failed.
  */
 OM_API int om_device_status(void *stream);
 
@@ -332,6 +357,15 @@ OM_API int om_device_status(void *stream);
  * other arguments, OM_ERR_CUDA on a launch error.
  */
 OM_API int om_selftest_wait_timeout(int which, int limit_ms, void *stream);
+
+/*
+ * om_selftest_wait_timeout reporting into a caller workspace: the timeout is
+ * recorded in the workspace's status word (om_workspace_status) and leaves
+ * the device-wide words untouched. Errors as om_selftest_wait_timeout, plus
+ * those of the workspace checks of om_gemm_f32_ws.
+ */
+OM_API int om_selftest_wait_timeout_ws(int which, int limit_ms, void *workspace,
+                                       size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }
