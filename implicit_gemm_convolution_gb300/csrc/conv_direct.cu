@@ -19,9 +19,11 @@
 // workload of the convolution page).
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 
 #include "om_device.cuh"
 #include "om_internal.h"
@@ -500,6 +502,279 @@ cudaError_t launch_skinny_mb(const DirectGeom &g, int mb, int64_t bands, int64_t
     }
 }
 
+// ---- depthwise KS x KS, "same" padding, stride 1 or 2, from a TMA window.
+// A block owns a band of RB output rows of one channel of one image. One
+// 4-D TMA copy (columns, rows, one channel, one image) brings the band's
+// input window into shared memory (rows 4 (mod 32) floats wide); the box
+// starts left of and above the plane as the padding needs and TMA writes +0
+// for every element outside it
+// (the zero border at copy time). Blocks are persistent: each walks its
+// (image, channel, band) items with kDwTmaStages window copies in flight, so
+// the copies of the next bands overlap this band's work. Thread s computes
+// the 8 consecutive
+// outputs of one strip of the band (row s % rows, columns 8 * (s / rows) ..): per
+// kernel row, 16-byte window loads and KS * 8 multiply-adds in (ky, kx)
+// order from +0, the weights in registers; the band's outputs are staged in
+// shared memory and leave in one coalesced pass with the epilogue.
+__device__ unsigned g_status_dw;
+
+struct DwTmaGeom {
+    float *y;
+    const float *w;
+    int OH, OW, Cout, w_ld;
+    int RB;    // output rows per band
+    int SPR;   // strips of 8 outputs per output row
+    int x0;    // first window column (a multiple of 4)
+    int BW, BH;
+    int N, bands;
+    int step_b, step_c, step_i;  // the grid size in (band, channel, image) digits
+    Epilogue ep;
+    unsigned *status;  // the call's status word in a caller workspace, or NULL
+};
+
+constexpr int kDwTmaMaxThreads = 512;
+constexpr int kDwTmaStages = 3;  // window copies in flight per block
+
+template <int MODE, int KS, int SW, int PAD>
+__global__ void __launch_bounds__(kDwTmaMaxThreads) conv_dw_tma_kernel(const __grid_constant__ CUtensorMap map,
+                                                                       const DwTmaGeom g) {
+    // window column of output column 0, kernel column 0: -PAD - x0; its
+    // offset in the 16-byte chunk every strip starts at
+    constexpr int kX0 = -4 * ((PAD + 3) / 4);
+    constexpr int C0 = -PAD - kX0;
+    constexpr int NV = 7 * SW + KS;             // window values of a strip's row
+    constexpr int NL = (C0 + NV + 3) / 4;       // 16-byte loads covering them
+    extern __shared__ uint8_t dw_raw[];
+    __shared__ uint64_t full[kDwTmaStages];
+    __shared__ int stop_sh;  // a window copy never landed: every thread leaves
+    uint8_t *ring = dw_raw + ((128u - (smem_u32(dw_raw) & 127u)) & 127u);
+    const uint32_t box_bytes = static_cast<uint32_t>(g.BW * g.BH) * 4u;
+    const uint32_t stage_bytes = (box_bytes + 127u) / 128u * 128u;
+    float *outs = reinterpret_cast<float *>(ring + kDwTmaStages * stage_bytes);  // RB x (OW + 4)
+    // items (image, channel, band), band fastest; this block takes
+    // blockIdx.x, blockIdx.x + gridDim.x, ... Item numbers advance by the
+    // grid size in mixed radix (band, channel, image), so no division is
+    // needed per item.
+    const int items = g.N * g.Cout * g.bands;
+    const int mine = static_cast<int>(blockIdx.x) < items
+                         ? (items - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                         : 0;
+    const int b0 = static_cast<int>(blockIdx.x) % g.bands;
+    const int c0 = (static_cast<int>(blockIdx.x) / g.bands) % g.Cout;
+    const int i0 = static_cast<int>(blockIdx.x) / (g.bands * g.Cout);
+    // the copy cursor (thread 0) runs kDwTmaStages items ahead of the compute cursor
+    int qb = b0, qc = c0, qi = i0;
+    auto advance = [&](int &b, int &c, int &i) {
+        b += g.step_b;
+        int carry = b >= g.bands;
+        b -= carry ? g.bands : 0;
+        c += g.step_c + carry;
+        carry = c >= g.Cout;
+        c -= carry ? g.Cout : 0;
+        i += g.step_i + carry;
+    };
+    auto issue = [&](int j) {
+        const int st = j % kDwTmaStages;
+        mbar_arrive_expect_tx(&full[st], box_bytes);
+        tma_load_4d(ring + st * stage_bytes, &map, &full[st], kX0, qb * g.RB * SW - PAD, qc, qi);
+        advance(qb, qc, qi);
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kDwTmaStages; ++st) mbar_init(&full[st], 1);
+        stop_sh = 0;
+        fence_mbar_init();
+        for (int j = 0; j < kDwTmaStages && j < mine; ++j) issue(j);
+    }
+    __syncthreads();
+    const int s = threadIdx.x;
+    // this thread's strip in a full band and in the last band (which may be
+    // shorter): lanes take consecutive rows of one strip column, so window
+    // rows 4 (mod 32) floats apart put a quarter-warp's 16-byte loads on
+    // distinct banks
+    const int rows_last = g.OH - (g.bands - 1) * g.RB;
+    const int seg_f = s / g.RB, ry_f = s - seg_f * g.RB;
+    const int seg_l = s / rows_last, ry_l = s - seg_l * rows_last;
+    int cb = b0, cc = c0, ci = i0;
+    for (int j = 0; j < mine; ++j) {
+        const bool last_band = cb == g.bands - 1;
+        const int rows = last_band ? rows_last : g.RB;
+        const int oy0 = cb * g.RB;
+        const int st = j % kDwTmaStages;
+        const bool landed = mbar_wait(&full[st], static_cast<uint32_t>((j / kDwTmaStages) & 1));
+        if (!landed) atomicOr(&stop_sh, 1);
+        if (landed && s < rows * g.SPR) {
+            float wk[KS * KS];
+#pragma unroll
+            for (int t = 0; t < KS * KS; ++t) wk[t] = __ldg(g.w + static_cast<int64_t>(cc) * g.w_ld + t);
+            const float *win = reinterpret_cast<const float *>(ring + st * stage_bytes);
+            const int ry = last_band ? ry_l : ry_f;
+            const int ox0 = (last_band ? seg_l : seg_f) * 8;
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+            for (int ky = 0; ky < KS; ++ky) {
+                const float4 *src = reinterpret_cast<const float4 *>(win + (ry * SW + ky) * g.BW + ox0 * SW);
+                float v[4 * NL];
+#pragma unroll
+                for (int q = 0; q < NL; ++q) {
+                    const float4 f = src[q];
+                    v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+                }
+#pragma unroll
+                for (int kx = 0; kx < KS; ++kx)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[q] = term<MODE>(acc[q], wk[ky * KS + kx], v[C0 + q * SW + kx]);
+            }
+            // staged by output row (pitch OW + 4 floats: a quarter-warp's
+            // rows on distinct banks); the band leaves in one coalesced pass
+            float4 *stg = reinterpret_cast<float4 *>(outs + ry * (g.OW + 4) + ox0);
+            stg[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            stg[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        __syncthreads();
+        if (landed) {
+            // the band's output rows oy0 .. oy0 + rows - 1 are one contiguous
+            // run of rows * OW floats in y
+            const int64_t ybase = ((static_cast<int64_t>(ci) * g.Cout + cc) * g.OH + oy0) * g.OW;
+            const int q4 = g.OW / 4;
+            const float *bias = g.ep.bias ? g.ep.bias + cc : nullptr;
+            const bool ep = g.ep.bias || g.ep.res || g.ep.act;
+            for (int e = s; e < rows * q4; e += blockDim.x) {
+                const int r = e / q4, c4 = e - r * q4;
+                float4 v = *reinterpret_cast<const float4 *>(outs + r * (g.OW + 4) + 4 * c4);
+                const int64_t o = ybase + static_cast<int64_t>(e) * 4;
+                if (ep) {
+                    const float *res = g.ep.res ? g.ep.res + o : nullptr;
+                    v.x = epilogue_value(v.x, bias, res, g.ep.act);
+                    v.y = epilogue_value(v.y, bias, res ? res + 1 : nullptr, g.ep.act);
+                    v.z = epilogue_value(v.z, bias, res ? res + 2 : nullptr, g.ep.act);
+                    v.w = epilogue_value(v.w, bias, res ? res + 3 : nullptr, g.ep.act);
+                }
+                *reinterpret_cast<float4 *>(g.y + o) =
+                    make_float4(canonical_nan(v.x), canonical_nan(v.y), canonical_nan(v.z), canonical_nan(v.w));
+            }
+        }
+        advance(cb, cc, ci);
+        // every thread's reads of this stage and of the staged outputs are
+        // done: hand the stage to the copy engine for the item kDwTmaStages
+        // ahead
+        __syncthreads();
+        if (*reinterpret_cast<volatile int *>(&stop_sh)) {
+            // copies still in flight land (or give up) before the block leaves
+            if (threadIdx.x == 0) {
+                report_timeout(g.status, &g_status_dw);
+                for (int jj = j; jj < mine && jj < j + kDwTmaStages; ++jj)
+                    (void)mbar_wait_limit(&full[jj % kDwTmaStages],
+                                          static_cast<uint32_t>((jj / kDwTmaStages) & 1), 1000000ull);
+            }
+            return;
+        }
+        if (threadIdx.x == 0 && j + kDwTmaStages < mine) {
+            fence_proxy_async_smem();
+            issue(j + kDwTmaStages);
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 dw_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+template <int MODE, int KS, int SW, int PAD>
+cudaError_t launch_dw_tma(const CUtensorMap &map, const DwTmaGeom &g, int threads, int smem, cudaStream_t s) {
+    auto kernel = conv_dw_tma_kernel<MODE, KS, SW, PAD>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    const int64_t items = static_cast<int64_t>(g.N) * g.Cout * g.bands;
+    int64_t grid = static_cast<int64_t>(num_sms()) * per_sm;
+    if (grid > items) grid = items;
+    DwTmaGeom gg = g;
+    gg.step_b = static_cast<int>(grid % g.bands);
+    gg.step_c = static_cast<int>((grid / g.bands) % g.Cout);
+    gg.step_i = static_cast<int>(grid / (static_cast<int64_t>(g.bands) * g.Cout));
+    kernel<<<static_cast<unsigned>(grid), threads, smem, s>>>(map, gg);
+    return cudaGetLastError();
+}
+
+// The TMA-window depthwise path; cudaErrorNotSupported when the shape is
+// not its own (then the 4-byte / 16-byte copy kernel below runs).
+cudaError_t launch_conv_depthwise_tma(const ConvProblem &p, int mode, cudaStream_t s) {
+    const int64_t ks = p.KH, sw = p.sH;
+    auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    if (p.pL != ks / 2 || p.pT != ks / 2) return cudaErrorNotSupported;
+    if (p.W % 4 != 0 || p.OW % 8 != 0 || !al16(p.x) || !al16(p.y) || (p.ep.res && !al16(p.ep.res)))
+        return cudaErrorNotSupported;
+    const int pad = static_cast<int>(p.pL);
+    const int x0 = -4 * ((pad + 3) / 4);
+    const int c0 = -pad - x0;
+    const int nl = (c0 + 7 * static_cast<int>(sw) + static_cast<int>(ks) + 3) / 4;
+    const int64_t spr = p.OW / 8;
+    // the last strip's loads reach window column 8 * (spr - 1) * sw + 4 * nl - 1;
+    // the box (and so the row pitch) is widened to 4 (mod 32) floats
+    int64_t bw = (8 * (spr - 1) * sw + 4 * nl + 3) / 4 * 4;
+    bw += ((4 - bw % 32) + 32) % 32;
+    if (bw > 256) return cudaErrorNotSupported;
+    // bands of at most 256 strips, as even as the rows allow
+    const int64_t rb_max = std::max<int64_t>(1, 256 / spr);
+    const int64_t nb = (p.OH + rb_max - 1) / rb_max;
+    const int64_t rb = (p.OH + nb - 1) / nb;
+    const int64_t bh = (rb - 1) * sw + ks;
+    if (bh > 256 || rb * spr > kDwTmaMaxThreads) return cudaErrorNotSupported;
+    auto fn = dw_encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.W), static_cast<cuuint64_t>(p.H),
+                          static_cast<cuuint64_t>(p.Cin), static_cast<cuuint64_t>(p.N)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.W) * 4, static_cast<cuuint64_t>(p.H * p.W) * 4,
+                             static_cast<cuuint64_t>(p.Cin * p.H * p.W) * 4};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(bw), static_cast<cuuint32_t>(bh), 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(p.x), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorNotSupported;
+    DwTmaGeom g{};
+    g.y = p.y;
+    g.w = p.w;
+    g.OH = static_cast<int>(p.OH);
+    g.OW = static_cast<int>(p.OW);
+    g.Cout = static_cast<int>(p.Cout);
+    g.w_ld = static_cast<int>(p.w_ld);
+    g.RB = static_cast<int>(rb);
+    g.SPR = static_cast<int>(spr);
+    g.x0 = x0;
+    g.BW = static_cast<int>(bw);
+    g.BH = static_cast<int>(bh);
+    g.N = static_cast<int>(p.N);
+    g.bands = static_cast<int>(nb);
+    g.ep = p.ep;
+    g.status = p.status;
+    const int threads = static_cast<int>((rb * spr + 31) / 32 * 32);
+    const int smem = static_cast<int>(kDwTmaStages * ((bw * bh * 4 + 127) / 128 * 128) + rb * (p.OW + 4) * 4 + 128);
+#define OM_DWT(K, S, P)                                                                               \
+    if (ks == K && sw == S && pad == P)                                                               \
+        return mode == kFast ? launch_dw_tma<kFast, K, S, P>(map, g, threads, smem, s) \
+                             : launch_dw_tma<kExact, K, S, P>(map, g, threads, smem, s);
+    OM_DWT(3, 1, 1) OM_DWT(3, 2, 1) OM_DWT(5, 1, 2) OM_DWT(5, 2, 2)
+#undef OM_DWT
+    return cudaErrorNotSupported;
+}
+
 }  // namespace
 
 int conv_direct_channels(int64_t M) {
@@ -513,6 +788,10 @@ namespace {
 // The depthwise KS x KS path: bands of R output rows whose window (rows of
 // Wp floats) fits in the block's shared memory.
 cudaError_t launch_conv_depthwise(const ConvProblem &p, int mode, cudaStream_t s) {
+    {
+        const cudaError_t e = launch_conv_depthwise_tma(p, mode, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     const int64_t ks = p.KH, sw = p.sH;
     // 16-byte window copies and output stores: input and output rows
     // 16-byte aligned (and the residual, when there is one)
@@ -695,6 +974,16 @@ cudaError_t launch_conv_skinny(const ConvProblem &p, int mode, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(floats(cc)) * 4;
     return mode == kFast ? launch_skinny_mb<kFast>(g, mb, bands, gy, p.N, smem, s)
                          : launch_skinny_mb<kExact>(g, mb, bands, gy, p.N, smem, s);
+}
+
+cudaError_t read_clear_status_dw(unsigned *out, cudaStream_t s) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status_dw, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (*out) e = cudaMemcpyToSymbol(g_status_dw, &zero, sizeof(unsigned));
+    return e;
 }
 
 }  // namespace om

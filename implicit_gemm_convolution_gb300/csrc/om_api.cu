@@ -444,14 +444,15 @@ int om_conv2d_f32_ex(int64_t N, int64_t Cin, int64_t H, int64_t W, int64_t Cout,
 
 int om_device_status(void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned a = 0, b = 0, c = 0, d = 0, e = 0, f = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0, e = 0, f = 0, h = 0;
     if (om::read_clear_status_gemm(&a, s) != cudaSuccess) return OM_ERR_CUDA;
+    if (om::read_clear_status_dw(&h, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_rows(&f, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_conv(&b, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_tc(&c, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_gemv(&d, s) != cudaSuccess) return OM_ERR_CUDA;
     if (om::read_clear_status_selftest(&e, s) != cudaSuccess) return OM_ERR_CUDA;
-    return ((a | b | c | d | e | f) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
+    return ((a | b | c | d | e | f | h) & om::kDevErrTimeoutHost) ? OM_ERR_TIMEOUT : OM_OK;
 }
 
 int om_selftest_wait_timeout(int which, int limit_ms, void *stream) {

@@ -89,6 +89,7 @@ constexpr int kConvDirectAutoM = 16;
 // (M rounded up to a power of two), or 0 above kConvDirectMaxM.
 int conv_direct_channels(int64_t M);
 cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s);
+cudaError_t read_clear_status_dw(unsigned *out, cudaStream_t s);
 // Few output pixels (output rows of at most 128 pixels), many output channels.
 cudaError_t launch_conv_skinny(const ConvProblem &p, int mode, cudaStream_t s);
 

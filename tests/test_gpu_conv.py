@@ -94,6 +94,14 @@ SMALL = [
     (2, 12, 21, 30, 12, 12, 5, 5, 2, 2, 1),
     (1, 8, 7, 7, 8, 8, 3, 3, 1, 0, 1),
     (1, 4, 300, 260, 4, 4, 3, 3, 1, 1, 1),
+    # depthwise with "same" padding, output rows a multiple of 8 (one TMA copy
+    # of the band's window): bands of 16 rows on a 112 x 112 plane, stride 2,
+    # 5 x 5, and a 16-column plane
+    (1, 8, 112, 112, 8, 8, 3, 3, 1, 1, 1),
+    (2, 6, 112, 112, 6, 6, 3, 3, 2, 1, 1),
+    (2, 4, 40, 40, 4, 4, 5, 5, 1, 2, 1),
+    (2, 4, 40, 48, 4, 4, 5, 5, 2, 2, 1),
+    (3, 16, 24, 16, 16, 16, 3, 3, 1, 1, 1),
     # rows a multiple of 4 floats (16-byte window copies and stores)
     (2, 8, 20, 32, 8, 8, 5, 5, 2, 2, 1),
     (2, 8, 30, 64, 8, 8, 3, 3, 2, 1, 1),

@@ -58,10 +58,12 @@ def ld_variants(cols):
     return [aligned, aligned + 1]
 
 
-# (m, n, k): at most 8 rows, strips of 64 columns with ragged tails, k
-# ragged against the 32-row stages, k below one stage
+# (m, n, k): at most 8 rows, column strips with ragged tails, k ragged
+# against the stages, k below one stage
 FEW_ROWS = [(1, 1, 1), (1, 300, 70), (2, 7, 31), (3, 1000, 300), (5, 129, 1), (8, 64, 33),
-            (8, 4097, 65), (6, 190, 1000)]
+            (8, 4097, 65), (6, 190, 1000),
+            # more 128-column strips than SMs: some blocks stream two strips
+            (2, 20000, 70)]
 # (m, n, k): at most 8 columns
 FEW_COLS = [(300, 1, 33), (1000, 1, 300), (65, 8, 33), (129, 3, 64), (70, 2, 1), (200, 5, 1001)]
 
