@@ -235,6 +235,43 @@ def time_reps(fn, flush, stream, min_ms: float = 80.0, reps: int = 3, warmup: in
             "calls_per_rep": calls}
 
 
+def time_rotating(fns, stream, min_ms: float = 80.0, reps: int = 3, warmup: int = 3) -> dict:
+    """Back-to-back calls cycling over fns, each working on its own copy of the
+    operands, with no flush in between: the copies are sized so that between
+    two calls on the same copy more data than the L2 holds passes through it,
+    so no call finds its operands in L2 (the 'inputs larger than L2' rule).
+    CUDA events bracket each batch on the launching stream, so launch latency
+    overlaps the previous call as it does for a caller issuing calls in a row;
+    a repetition's figure is batch time / calls, the result the median."""
+    import torch
+    n = len(fns)
+    for i in range(max(warmup, n)):
+        fns[i % n]()
+    torch.cuda.synchronize()
+
+    def batch(calls):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(calls):
+            fns[i % n]()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
+    probe = batch(2 * n) / (2 * n)
+    calls = max(2 * n, int(np.ceil(min_ms / max(probe, 1e-4) / n)) * n)
+    means = [batch(calls) / calls for _ in range(reps)]
+    return {"ms": float(np.median(means)), "rep_ms": [round(v, 5) for v in means],
+            "calls_per_rep": [calls] * reps, "copies": n}
+
+
+def rotation_copies(nbytes: float, l2_bytes: float) -> int:
+    """Operand copies for time_rotating: the fewest with (copies - 1) x the
+    call's bytes >= 1.5 x the L2 size."""
+    return max(2, int(np.ceil(1.5 * l2_bytes / nbytes)) + 1)
+
+
 def combine_ranks(ms_local: float, flops_per_rank: float, world: int, dist=None, device="cpu"):
     """Replicas only: every rank ran the same workload on its own GPU with no
     exchange. Returns (the slowest rank's ms per step, whole-job GFLOP/s =
@@ -391,19 +428,21 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     extras = {}
 
     wsp = om.new_workspace(dev)
+    l2_bytes = float(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129e6)
 
     def gemm_line(name, mode, case_, use_ws=False, hbm_bound=False):
-        Ad = torch.from_numpy(case_.A).to(dev)
-        Bd = torch.from_numpy(case_.B).to(dev)
-        Cd = torch.from_numpy(case_.C_init).to(dev)
-
-        def f():
-            st = om.gemm_raw(case_.m, case_.n, case_.k, Ad.data_ptr(), case_.lda, Bd.data_ptr(),
-                             case_.ldb, Cd.data_ptr(), case_.ldc, mode, stream,
-                             workspace=wsp if use_ws else None)
-            if st != 0:
-                raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
-        r = time_reps(f, flush, stream, args.rep_ms)
+        def make(Ad, Bd, Cd):
+            def f():
+                st = om.gemm_raw(case_.m, case_.n, case_.k, Ad.data_ptr(), case_.lda, Bd.data_ptr(),
+                                 case_.ldb, Cd.data_ptr(), case_.ldc, mode, stream,
+                                 workspace=wsp if use_ws else None)
+                if st != 0:
+                    raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
+            return f
+        ops = (torch.from_numpy(case_.A).to(dev), torch.from_numpy(case_.B).to(dev),
+               torch.from_numpy(case_.C_init).to(dev))
+        t0 = time.time()
+        r = time_reps(make(*ops), flush, stream, args.rep_ms)
         t = r["ms"]
         fl = 2.0 * case_.m * case_.n * case_.k
         tf = fl / (t * 1e-3) / 1e12
@@ -412,16 +451,38 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2),
                         "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"]}
         if hbm_bound:
-            extras[name].update(hbm_fields(4.0 * (case_.m * case_.k + case_.k * case_.n +
-                                                  case_.m * case_.n), t))
+            nbytes = 4.0 * (case_.m * case_.k + case_.k * case_.n + case_.m * case_.n)
+            copies = [ops] + [tuple(torch.empty_like(o).copy_(o) for o in ops)
+                              for _ in range(rotation_copies(nbytes, l2_bytes) - 1)]
+            rr = time_rotating([make(*o) for o in copies], stream, args.rep_ms)
+            extras[name].update(hbm_fields(nbytes, t, rr))
+            del copies
+        extras[name]["clocks"] = line_clocks(t0)
 
-    def hbm_fields(nbytes, t_ms):
+    def hbm_fields(nbytes, t_flushed, rot):
         """Algorithmic bytes (each operand read once, the output written once)
-        against the measured copy bandwidth, for HBM-bound kernels."""
-        gbs = nbytes / (t_ms * 1e-3) / 1e9
+        against the measured copy bandwidth, for HBM-bound kernels. The
+        figure is taken from calls in a row rotating over operand copies
+        larger than L2 (time_rotating); the per-call figure with L2 flushed
+        before each call, which adds the launch latency and the write-back of
+        the flush's dirty lines to every call, is kept beside it."""
+        gbs = nbytes / (rot["ms"] * 1e-3) / 1e9
         hbm = measured_peaks()["hbm_gbs"]
-        return {"bound": "hbm", "GB/s": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
-                "hbm_peak_gbs": hbm, "algorithmic_bytes": int(nbytes)}
+        gbs_f = nbytes / (t_flushed * 1e-3) / 1e9
+        return {"bound": "hbm", "ms_in_a_row": round(rot["ms"], 4), "GB/s": round(gbs, 1),
+                "hbm_frac": round(gbs / hbm, 4), "hbm_peak_gbs": hbm, "algorithmic_bytes": int(nbytes),
+                "timing": f"calls in a row over {rot['copies']} operand copies of {nbytes / 1e6:.0f} MB "
+                          f"each (L2 {l2_bytes / 1e6:.0f} MB), no flush; median of 3 repetitions "
+                          f"of >= {args.rep_ms:.0f} ms",
+                "rep_ms_in_a_row": rot["rep_ms"],
+                "GB/s_flushed_per_call": round(gbs_f, 1), "hbm_frac_flushed_per_call": round(gbs_f / hbm, 4)}
+
+    clock_log = ClockSampler(local_rank)
+    clock_log.__enter__()
+
+    def line_clocks(t0):
+        c = clock_log.summary(t0, time.time())
+        return {"sm_mhz": c["sm_mhz"], "reasons": c["reasons"], "samples": c["samples"]}
 
     def tf32x3_line(name, case_):
         Ad = torch.from_numpy(case_.A).to(dev)
@@ -433,6 +494,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                              case_.ldb, Cd.data_ptr(), case_.ldc, "tf32x3", stream)
             if st != 0:
                 raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
+        t0 = time.time()
         r = time_reps(f, flush, stream, args.rep_ms)
         t = r["ms"]
         fl = 2.0 * case_.m * case_.n * case_.k
@@ -445,27 +507,30 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "tensor_peak_tflops": round(tf32_peak, 1),
                         "tensor_peak_basis": peaks["basis"] + " x nominal tf32/bf16 ratio 1.1/2.25; "
                                              "three tensor-core products per useful flop",
-                        "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"]}
+                        "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"],
+                        "clocks": line_clocks(t0)}
 
     def conv_line(name, mode, c, use_ws=False, hbm_bound=False):
-        x = torch.from_numpy(c.x).to(dev)
-        w = torch.from_numpy(c.w).to(dev)
         OH = om.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.dil)
         OW = om.conv_out_dim(c.W, c.KW, c.stride, c.pad, c.dil)
-        y = torch.empty((c.N, c.Cout, OH, OW), dtype=torch.float32, device=dev)
         L = om.lib()
 
-        def f():
-            args = (c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad, c.dil,
-                    x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[mode])
-            if use_ws:
-                st = L.om_conv2d_f32_ws(*args, wsp.data_ptr(), om.workspace_bytes(),
-                                        stream.cuda_stream)
-            else:
-                st = L.om_conv2d_f32(*args, stream.cuda_stream)
-            if st != 0:
-                raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
-        r = time_reps(f, flush, stream, args.rep_ms)
+        def make(x, w, y):
+            def f():
+                args_ = (c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad, c.dil,
+                         x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[mode])
+                if use_ws:
+                    st = L.om_conv2d_f32_ws(*args_, wsp.data_ptr(), om.workspace_bytes(),
+                                            stream.cuda_stream)
+                else:
+                    st = L.om_conv2d_f32(*args_, stream.cuda_stream)
+                if st != 0:
+                    raise RuntimeError(f"{name}: {om.STATUS_NAMES.get(st, st)}")
+            return f
+        ops = (torch.from_numpy(c.x).to(dev), torch.from_numpy(c.w).to(dev),
+               torch.empty((c.N, c.Cout, OH, OW), dtype=torch.float32, device=dev))
+        t0 = time.time()
+        r = time_reps(make(*ops), flush, stream, args.rep_ms)
         t = r["ms"]
         fl = 2.0 * c.N * c.Cout * OH * OW * (c.Cin // c.G) * c.KH * c.KW
         tf = fl / (t * 1e-3) / 1e12
@@ -474,7 +539,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "roofline_frac": round(tf / pk, 4), "peak_tflops": round(pk, 2),
                         "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"]}
         if hbm_bound:
-            extras[name].update(hbm_fields(4.0 * (c.x.size + c.w.size + c.N * c.Cout * OH * OW), t))
+            nbytes = 4.0 * (c.x.size + c.w.size + c.N * c.Cout * OH * OW)
+            copies = [ops] + [tuple(torch.empty_like(o).copy_(o) for o in ops)
+                              for _ in range(rotation_copies(nbytes, l2_bytes) - 1)]
+            rr = time_rotating([make(*o) for o in copies], stream, args.rep_ms)
+            extras[name].update(hbm_fields(nbytes, t, rr))
+            del copies
+        extras[name]["clocks"] = line_clocks(t0)
 
     def chain_line(name, mode):
         """ResNet-50's 53 convolutions at 224 x 224, batch 1, each with its
@@ -483,6 +554,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         from implicit_gemm_convolution_gb300 import chain
         ch = chain.ConvChain(chain.resnet50_convs(), 1, 224, mode, device=dev)
         graph = ch.capture()
+        t0 = time.time()
         t_graph = time_reps(graph.replay, flush, stream, args.rep_ms)["ms"]
         t_eager = time_reps(ch.run, flush, stream, args.rep_ms)["ms"]
         tf = ch.flops / (t_graph * 1e-3) / 1e12
@@ -492,7 +564,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "peak_tflops": round(pk, 2), "layers": len(ch.layers),
                         "gflop": round(ch.flops / 1e9, 3),
                         "context": "the pages' ResNet-50 convolution chain, 16/32 CPU threads on a "
-                                   "16-core Zen 4: 12.3/11.1 ms (other hardware)"}
+                                   "16-core Zen 4: 12.3/11.1 ms (other hardware)",
+                        "clocks": line_clocks(t0)}
 
     if not args.headline_only:
         gemm_line("gemm_4096^3_fast_ws", "fast", case, use_ws=True)
@@ -531,6 +604,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         for md in ("exact", "fast"):
             chain_line(f"resnet50_conv_chain_b1_224_{md}", md)
 
+    clock_log.__exit__(None, None, None)
     cpu = cpu_baseline(args.cpu_seconds)
     line = {
         "metric": "GFLOP/s and % of FP32 CUDA-core roofline per mode (GEMM 4096^3; conv3x3)",

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kSkinnyThreads) conv_skinny_kernel(const Direc
     const int rows = min(g.R, g.OH - oy0);
     const int wr = (rows - 1) * g.sH + (g.KH - 1) * g.dH + 1;
     const int iy_base = oy0 * g.sH - g.pT;
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int tid = threadIdx.x;
     const int taps = g.KH * g.KW;
     const int cc_max = g.R_chunk;  // channels per chunk
     const int nchunks = (g.cin_g + cc_max - 1) / cc_max;
@@ -775,6 +775,133 @@ cudaError_t launch_conv_depthwise_tma(const ConvProblem &p, int mode, cudaStream
     return cudaErrorNotSupported;
 }
 
+// ---- groups of a few output channels (M <= 16) with KS x KS taps from a
+// TMA window. A block owns a band of R output rows of one group of one
+// image. One 4-D TMA copy (columns, rows, the group's input channels, one
+// image) lands the band's input window in shared memory, rows BW floats
+// wide, the box starting left of and above the plane as the padding needs,
+// TMA writing +0 for every element outside the plane (the zero border at
+// copy time); the group's weights arrive meanwhile by plain loads, stored
+// tap-major (MT = OB * MB per tap, +0 past M). Thread u computes one output
+// pixel of the band for one block of MB of the group's channels (OB blocks;
+// a warp's threads share the block, so the weights of a tap are one
+// broadcast read): per input channel and tap, in (c, ky, kx) order, the MB
+// products of the window value and the tap's weights, so each output is one
+// accumulator from +0 over (c, ky, kx) in the pages' order.
+constexpr int kGrpMaxThreads = 256;
+
+struct GrpGeom {
+    float *y;
+    const float *w;
+    int OH, OW, P, Cout, M, K, w_ld, cin_g;
+    int R;               // output rows per band
+    int OB, MT;          // channel blocks of MB per pixel; channel slots OB * MB
+    int BW, BH;          // window row pitch (= box width) and rows per channel
+    int sH, sW, dH, dW;
+    int pT, x0, c0;      // box origin column x0 (a multiple of 4); window column of input column -pL
+    Epilogue ep;
+    unsigned *status;
+};
+
+template <int MODE, int MB, int KS>
+__global__ void __launch_bounds__(kGrpMaxThreads) conv_group_kernel(const __grid_constant__ CUtensorMap map,
+                                                                    const GrpGeom g) {
+    static_assert(MB % 4 == 0, "weights per tap are read 16 bytes at a time");
+    extern __shared__ uint8_t gw_raw[];
+    __shared__ uint64_t full;
+    float *win = reinterpret_cast<float *>(gw_raw + ((128u - (smem_u32(gw_raw) & 127u)) & 127u));
+    const int plane = g.BH * g.BW;
+    const uint32_t win_bytes = static_cast<uint32_t>(g.cin_g * plane) * 4u;
+    float *wsm = win + (g.cin_g * plane + 3) / 4 * 4;
+    const int grp = blockIdx.y, img = blockIdx.z;
+    const int oy0 = blockIdx.x * g.R;
+    if (threadIdx.x == 0) {
+        mbar_init(&full, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&full, win_bytes);
+        tma_load_4d(win, &map, &full, g.x0, oy0 * g.sH - g.pT, grp * g.cin_g, img);
+    }
+    // the group's weight rows, read along the taps (coalesced) while the
+    // window is in flight, stored tap-major (+0 past M)
+    {
+        const float *wg = g.w + static_cast<int64_t>(grp) * g.M * g.w_ld;
+        for (int i = threadIdx.x; i < g.MT * g.K; i += blockDim.x) {
+            const int oc = i / g.K, t = i - oc * g.K;
+            wsm[t * g.MT + oc] = oc < g.M ? __ldg(wg + static_cast<int64_t>(oc) * g.w_ld + t) : 0.0f;
+        }
+    }
+    __syncthreads();
+    const bool landed = mbar_wait(&full, 0);
+    if (!landed) {
+        if (threadIdx.x == 0) {
+            report_timeout(g.status, &g_status_dw);
+            // the copy, if it is still in flight, lands (or gives up) before the block leaves
+            (void)mbar_wait_limit(&full, 0, 1000000ull);
+        }
+        return;
+    }
+    const int rows = min(g.R, g.OH - oy0);
+    // thread u: channel block u / (R * OW), pixel u % (R * OW)
+    const int ob = threadIdx.x / (g.R * g.OW);
+    const int u = threadIdx.x - ob * (g.R * g.OW);
+    if (ob >= g.OB || u >= rows * g.OW) return;
+    const int ry = u / g.OW, ox = u - ry * g.OW;
+    const float *src = win + ry * g.sH * g.BW + ox * g.sW + g.c0;
+    int off[KS * KS];
+#pragma unroll
+    for (int ky = 0; ky < KS; ++ky)
+#pragma unroll
+        for (int kx = 0; kx < KS; ++kx) off[ky * KS + kx] = ky * g.dH * g.BW + kx * g.dW;
+    float2 acc[MB / 2];
+#pragma unroll
+    for (int h = 0; h < MB / 2; ++h) acc[h] = make_float2(0.0f, 0.0f);
+    const float *wblk = wsm + ob * MB;
+#pragma unroll 1
+    for (int c = 0; c < g.cin_g; ++c) {
+        const float *sc = src + c * plane;
+        const float4 *wt = reinterpret_cast<const float4 *>(wblk + c * (KS * KS * g.MT));
+        float v[KS * KS];
+#pragma unroll
+        for (int t = 0; t < KS * KS; ++t) v[t] = sc[off[t]];
+#pragma unroll
+        for (int t = 0; t < KS * KS; ++t) {
+            const float2 vv = make_float2(v[t], v[t]);
+#pragma unroll
+            for (int q = 0; q < MB / 4; ++q) {
+                const float4 w4 = wt[t * (g.MT / 4) + q];
+                acc[2 * q] = term2<MODE>(acc[2 * q], make_float2(w4.x, w4.y), vv);
+                acc[2 * q + 1] = term2<MODE>(acc[2 * q + 1], make_float2(w4.z, w4.w), vv);
+            }
+        }
+    }
+    const int oc0 = ob * MB;
+    const int64_t o0 = (static_cast<int64_t>(img) * g.Cout + static_cast<int64_t>(grp) * g.M + oc0) * g.P +
+                       static_cast<int64_t>(oy0 + ry) * g.OW + ox;
+    const bool ep = g.ep.bias || g.ep.res || g.ep.act;
+#pragma unroll
+    for (int oc = 0; oc < MB; ++oc) {
+        if (oc0 + oc < g.M) {
+            float v = (oc & 1) ? acc[oc / 2].y : acc[oc / 2].x;
+            const int64_t o = o0 + static_cast<int64_t>(oc) * g.P;
+            if (ep)
+                v = epilogue_value(v, g.ep.bias ? g.ep.bias + grp * g.M + oc0 + oc : nullptr,
+                                   g.ep.res ? g.ep.res + o : nullptr, g.ep.act);
+            g.y[o] = canonical_nan(v);
+        }
+    }
+}
+
+template <int MODE, int MB, int KS>
+cudaError_t launch_group(const CUtensorMap &map, const GrpGeom &g, int bands, int groups, int images, int threads,
+                         int smem, cudaStream_t s) {
+    auto kernel = conv_group_kernel<MODE, MB, KS>;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3(static_cast<unsigned>(bands), static_cast<unsigned>(groups), static_cast<unsigned>(images)),
+             threads, smem, s>>>(map, g);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 int conv_direct_channels(int64_t M) {
@@ -845,6 +972,99 @@ cudaError_t launch_conv_depthwise(const ConvProblem &p, int mode, cudaStream_t s
 }
 
 }  // namespace
+
+cudaError_t launch_conv_group(const ConvProblem &p, int mode, cudaStream_t s) {
+    const int64_t M = p.Cout / p.G, cin_g = p.Cin / p.G;
+    const int64_t ks = p.KH;
+    auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    if (M < 1 || M > 16 || (M == 1 && cin_g == 1) || p.KW != ks || (ks != 1 && ks != 3 && ks != 5))
+        return cudaErrorNotSupported;
+    if (p.N == 0 || p.OH * p.OW == 0) return cudaSuccess;
+    // one TMA box per band: rows 16-byte aligned, every box dimension <= 256
+    constexpr int64_t kCoordMax = int64_t{1} << 24;
+    if (p.W % 4 != 0 || !al16(p.x) || cin_g > 256 || p.H > kCoordMax || p.W > kCoordMax || p.pT > 1024 ||
+        p.pL > 1024 || p.sH * p.dH > kCoordMax || p.sW * p.dW > kCoordMax || p.N > 65535 || p.G > 65535 ||
+        p.w_ld > 0x7FFFFFFF || p.Cout * p.OH * p.OW > 0x7FFFFFFF)
+        return cudaErrorNotSupported;
+    const int64_t mb = M <= 4 ? 4 : 8, ob = (M + mb - 1) / mb;
+    if (ob * p.OW > kGrpMaxThreads) return cudaErrorNotSupported;
+    const int64_t x0 = -4 * ((p.pL + 3) / 4);
+    const int64_t c0 = -p.pL - x0;
+    // the last pixel's last tap reads window column c0 + (OW-1)*sW + (KW-1)*dW
+    const int64_t bw = (c0 + (p.OW - 1) * p.sW + (ks - 1) * p.dW + 1 + 3) / 4 * 4;
+    if (bw > 256) return cudaErrorNotSupported;
+    const int64_t wfloats = p.K * ob * mb;
+    auto bh_of = [&](int64_t R) { return (R - 1) * p.sH + (ks - 1) * p.dH + 1; };
+    auto smem_for = [&](int64_t R) { return 128 + ((cin_g * bh_of(R) * bw + 3) / 4 * 4 + wfloats) * 4; };
+    auto rows_ok = [&](int64_t R) {
+        return ob * R * p.OW <= kGrpMaxThreads && bh_of(R) <= 256 && smem_for(R) <= 100 * 1024;
+    };
+    if (!rows_ok(1)) return cudaErrorNotSupported;
+    // the most output rows per band that fit, evened out over the bands; then
+    // more, shorter bands while the grid has fewer than two blocks per SM
+    int64_t R = std::min<int64_t>(p.OH, kGrpMaxThreads / (ob * p.OW));
+    while (R > 1 && !rows_ok(R)) --R;
+    int64_t bands = (p.OH + R - 1) / R;
+    R = (p.OH + bands - 1) / bands;
+    const int64_t planes = p.N * p.G;
+    const int64_t want = 2 * static_cast<int64_t>(num_sms());
+    if (planes * bands < want) {
+        bands = std::min<int64_t>(p.OH, (want + planes - 1) / planes);
+        R = (p.OH + bands - 1) / bands;
+        bands = (p.OH + R - 1) / R;
+    }
+    const int64_t bh = bh_of(R);
+    auto fn = dw_encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(p.W), static_cast<cuuint64_t>(p.H),
+                          static_cast<cuuint64_t>(p.Cin), static_cast<cuuint64_t>(p.N)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.W) * 4, static_cast<cuuint64_t>(p.H * p.W) * 4,
+                             static_cast<cuuint64_t>(p.Cin * p.H * p.W) * 4};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(bw), static_cast<cuuint32_t>(bh),
+                         static_cast<cuuint32_t>(cin_g), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(p.x), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorNotSupported;
+    GrpGeom g{};
+    g.y = p.y;
+    g.w = p.w;
+    g.OH = static_cast<int>(p.OH);
+    g.OW = static_cast<int>(p.OW);
+    g.P = static_cast<int>(p.OH * p.OW);
+    g.Cout = static_cast<int>(p.Cout);
+    g.M = static_cast<int>(M);
+    g.K = static_cast<int>(p.K);
+    g.w_ld = static_cast<int>(p.w_ld);
+    g.cin_g = static_cast<int>(cin_g);
+    g.R = static_cast<int>(R);
+    g.OB = static_cast<int>(ob);
+    g.MT = static_cast<int>(ob * mb);
+    g.BW = static_cast<int>(bw);
+    g.BH = static_cast<int>(bh);
+    g.sH = static_cast<int>(p.sH);
+    g.sW = static_cast<int>(p.sW);
+    g.dH = static_cast<int>(p.dH);
+    g.dW = static_cast<int>(p.dW);
+    g.pT = static_cast<int>(p.pT);
+    g.x0 = static_cast<int>(x0);
+    g.c0 = static_cast<int>(c0);
+    g.ep = p.ep;
+    g.status = p.status;
+    const int threads = static_cast<int>(std::max<int64_t>(32, (ob * R * p.OW + 31) / 32 * 32));
+    const int smem = static_cast<int>(smem_for(R));
+    const int nb = static_cast<int>(bands), ng = static_cast<int>(p.G), ni = static_cast<int>(p.N);
+#define OM_GR(MB_, KS_)                                                                          \
+    if (mb == MB_ && ks == KS_)                                                                  \
+        return mode == kFast ? launch_group<kFast, MB_, KS_>(map, g, nb, ng, ni, threads, smem, s) \
+                             : launch_group<kExact, MB_, KS_>(map, g, nb, ng, ni, threads, smem, s);
+    OM_GR(4, 1) OM_GR(4, 3) OM_GR(4, 5) OM_GR(8, 1) OM_GR(8, 3) OM_GR(8, 5)
+#undef OM_GR
+    return cudaErrorNotSupported;
+}
 
 cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s) {
     const int64_t M = p.Cout / p.G;

@@ -173,6 +173,9 @@ int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     cudaError_t e = cudaErrorNotSupported;
     if (cfg == om::kConvGemv || cfg < 0) e = om::launch_conv_gemv(p, mode, s);
     if (e == cudaErrorNotSupported &&
+        (cfg == om::kConvGroup || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM)))
+        e = om::launch_conv_group(p, mode, s);
+    if (e == cudaErrorNotSupported &&
         (cfg == om::kConvDirect || (cfg < 0 && p.Cout / p.G <= om::kConvDirectAutoM)))
         e = om::launch_conv_direct(p, mode, s);
     if (e == cudaErrorNotSupported && (cfg == om::kConvRows || cfg < 0))
@@ -182,7 +185,8 @@ int run_conv(const ConvProblem &p, int mode, unsigned *flags, cudaStream_t s) {
     if (e == cudaErrorNotSupported && (cfg == om::kConvSkinny || (cfg < 0 && few_pixels(p))))
         e = om::launch_conv_skinny(p, mode, s);
     if (e == cudaErrorNotSupported && cfg != om::kConvDirect && cfg != om::kConvGemv &&
-        cfg != om::kConvSkinny && cfg != om::kConvColumns && cfg != om::kConvRows)
+        cfg != om::kConvSkinny && cfg != om::kConvColumns && cfg != om::kConvRows &&
+        cfg != om::kConvGroup)
         e = om::launch_conv_implicit(p, mode, cfg < 0 ? om::kConvAuto : cfg, flags, s);
     if (e == cudaErrorNotSupported) e = om::launch_conv_naive(p, mode, s);
     return from_cuda(e);

@@ -77,6 +77,7 @@ enum ConvCfg : int {
     kConvSkinny = 4,    // few output pixels: one pixel per thread, channels streamed in chunks
     kConvColumns = 5,   // blocks of 32 channels x 8 pixels, weights by TMA, patches gathered
     kConvRows = 6,      // stride 1: warps own output-row segments of 64 channels, windows by TMA
+    kConvGroup = 7,     // up to 16 channels per group, KS x KS taps: a band's window by one TMA copy
 };
 
 // The direct kernel serves groups of up to kConvDirectMaxM output channels
@@ -89,6 +90,11 @@ constexpr int kConvDirectAutoM = 16;
 // (M rounded up to a power of two), or 0 above kConvDirectMaxM.
 int conv_direct_channels(int64_t M);
 cudaError_t launch_conv_direct(const ConvProblem &p, int mode, cudaStream_t s);
+// Groups of at most 16 output channels with 1x1, 3x3 or 5x5 taps (any
+// stride, dilation and padding) whose input rows are 16-byte aligned: one
+// block per band of output rows of one group and image, its input window
+// copied by one TMA load with zero fill; cudaErrorNotSupported otherwise.
+cudaError_t launch_conv_group(const ConvProblem &p, int mode, cudaStream_t s);
 cudaError_t read_clear_status_dw(unsigned *out, cudaStream_t s);
 // Few output pixels (output rows of at most 128 pixels), many output channels.
 cudaError_t launch_conv_skinny(const ConvProblem &p, int mode, cudaStream_t s);

@@ -11,8 +11,9 @@ from tests.gpu_util import (assert_bits_equal, forced_config, guarded_output, gu
 pytestmark = pytest.mark.gpu
 
 MODES = [(oracle.EXACT, "exact"), (oracle.FAST, "fast")]
-# naive, implicit GEMM, direct small-group, few-pixel, 1x1 columns, row segments, default
-CFGS = [0, 1, 2, 4, 5, 6, None]
+# naive, implicit GEMM, direct small-group, few-pixel, 1x1 columns, row
+# segments, small-group TMA window, default
+CFGS = [0, 1, 2, 4, 5, 6, 7, None]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -125,6 +126,21 @@ SMALL = [
     (4, 20, 14, 14, 256, 1, 1, 1, 1, 0, 1),
     (2, 72, 8, 56, 64, 1, 3, 3, 1, 1, 1),
     (2, 37, 8, 56, 64, 1, 1, 1, 1, 0, 1),
+    # the small-group TMA window kernel's shapes (input rows a multiple of 4
+    # floats): 1, 2, 4, 6, 12 and 16 channels per group (4, 8 and 16 channel
+    # slots); 1x1, 3x3, 5x5; stride 2 with dilation 2; paddings 0, 4 and 5
+    # (window origins 0, -4 and -8 columns); several bands with a short last
+    # one; a 248-pixel output row
+    (2, 32, 16, 16, 32, 8, 3, 3, 1, 1, 1),
+    (2, 24, 12, 20, 48, 8, 3, 3, 2, 1, 2),
+    (1, 64, 20, 24, 64, 4, 3, 3, 1, 1, 1),
+    (2, 16, 12, 12, 48, 4, 5, 5, 1, 2, 1),
+    (3, 12, 8, 8, 6, 3, 1, 1, 1, 0, 1),
+    (2, 8, 9, 16, 4, 4, 3, 3, 2, 0, 1),
+    (1, 32, 40, 40, 48, 16, 3, 3, 1, 1, 1),
+    (1, 8, 10, 12, 8, 2, 3, 3, 1, 4, 1),
+    (1, 6, 7, 8, 6, 3, 3, 3, 2, 5, 2),
+    (2, 16, 6, 248, 16, 4, 3, 3, 1, 1, 1),
 ]
 
 
@@ -248,8 +264,10 @@ def test_1x1_input_not_16_byte_aligned(mode, name):
     assert_bits_equal(y.cpu().numpy(), want_conv(c, mode), "misaligned 1x1")
 
 
-# Shapes with enough output pixels that the direct small-group kernel gives
-# each thread 4 (depthwise; 8 channels per group) or 2 (4 channels) pixels.
+# Shapes with enough output pixels that the direct small-group kernel
+# (forced as configuration 2) gives each thread 4 (depthwise; 8 channels per
+# group) or 2 (4 channels) pixels; by default the TMA window kernel takes the
+# grouped ones.
 DIRECT_WIDE = [
     (4, 64, 56, 56, 64, 64, 3, 3, 1, 1, 1),
     (4, 128, 48, 48, 256, 64, 3, 3, 1, 1, 1),
@@ -258,8 +276,34 @@ DIRECT_WIDE = [
 
 
 @pytest.mark.parametrize("shape", DIRECT_WIDE)
+@pytest.mark.parametrize("cfg", [2, None])
 @pytest.mark.parametrize("mode,name", MODES)
-def test_direct_kernel_several_pixels_per_thread(shape, mode, name):
+def test_direct_kernel_several_pixels_per_thread(shape, mode, name, cfg):
     c = synth.make_conv("t", *shape, seed=sum(shape) + 5, dist_x=("uniform", -1, 1),
                         dist_w=("normal", 0, 0.5))
-    assert_bits_equal(run_conv(c, name), want_conv(c, mode), f"direct {shape}")
+    assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"direct {shape} cfg={cfg}")
+
+
+# Larger shapes of the small-group TMA window kernel: 4 and 8 channel
+# slots per thread, 16-channel groups in two blocks of 8, several bands per
+# plane, 1x1 / 3x3 / 5x5, stride and dilation 1 or 2.
+GROUP_WIDE = [
+    (8, 64, 30, 28, 64, 16, 3, 3, 1, 1, 1),
+    (32, 64, 40, 40, 64, 8, 3, 3, 2, 1, 1),
+    (4, 64, 36, 36, 128, 8, 5, 5, 1, 2, 1),
+    (8, 64, 32, 64, 32, 16, 1, 1, 1, 0, 1),
+    (4, 64, 36, 36, 128, 8, 3, 3, 1, 2, 2),
+    (20, 96, 26, 28, 96, 24, 3, 3, 2, 1, 2),
+    (64, 64, 40, 40, 64, 8, 3, 3, 2, 1, 1),
+    (16, 128, 32, 64, 128, 16, 1, 1, 1, 0, 1),
+    (8, 64, 36, 36, 128, 16, 5, 5, 1, 2, 1),
+]
+
+
+@pytest.mark.parametrize("shape", GROUP_WIDE)
+@pytest.mark.parametrize("cfg", [7, None])
+@pytest.mark.parametrize("mode,name", MODES)
+def test_group_window_kernel_wide_shapes(shape, mode, name, cfg):
+    c = synth.make_conv("t", *shape, seed=sum(shape) + 9, dist_x=("uniform", -1, 1),
+                        dist_w=("normal", 0, 0.5))
+    assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"group window {shape} cfg={cfg}")

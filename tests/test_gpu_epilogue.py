@@ -65,6 +65,8 @@ CONVS = [
     (1, 8, 13, 13, 8, 8, 3, 3, 2, 1, 2),
     # the row-segment kernel's shape (forced below as configuration 6)
     (2, 8, 8, 28, 64, 1, 3, 3, 1, 1, 1),
+    # small groups (the direct kernel and the TMA window kernel, configurations 2 and 7)
+    (2, 32, 12, 16, 48, 8, 3, 3, 2, 1, 2),
 ]
 
 
@@ -82,7 +84,7 @@ def test_conv_epilogue(shape, mode, name):
     x, w, db, dr = to_dev(c.x), to_dev(c.w), to_dev(bias), to_dev(res)
     wp = om.pack_conv_weights(w, G)
     ws = om.new_workspace()
-    for cfg in (None, 0, 1, 6):
+    for cfg in (None, 0, 1, 2, 6, 7):
         for workspace in (None, ws):
             for packed in (False, True):
                 with forced_config("OM_FORCE_CONV_CFG", cfg):
