@@ -144,6 +144,8 @@ KERNEL_SOURCES = {
     "gemm_tf32x3_kernel": ("gemm_tf32x3.cu", "om_device.cuh", "om_internal.h"),
     "conv_rows_kernel": ("conv_rows.cu", "om_device.cuh", "om_internal.h"),
     "gemv_kernel": ("gemv.cu", "om_device.cuh", "om_internal.h"),
+    "conv_dw_tma_kernel": ("conv_direct.cu", "om_device.cuh", "om_internal.h"),
+    "conv_group_kernel": ("conv_direct.cu", "om_device.cuh", "om_internal.h"),
 }
 
 
@@ -430,7 +432,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     wsp = om.new_workspace(dev)
     l2_bytes = float(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129e6)
 
-    def gemm_line(name, mode, case_, use_ws=False, hbm_bound=False):
+    def with_traffic(name, traffic):
+        """DRAM bytes per launch of the line's kernel from the committed ncu
+        capture of the same workload (None when that capture is older than the
+        kernel's sources)."""
+        if traffic is not None:
+            extras[name]["traffic"] = recorded_traffic(*traffic)
+            extras[name]["traffic_source"] = f"{traffic[0]} {traffic[1]}, profiles/dram_traffic.txt"
+
+    def gemm_line(name, mode, case_, use_ws=False, hbm_bound=False, traffic=None):
         def make(Ad, Bd, Cd):
             def f():
                 st = om.gemm_raw(case_.m, case_.n, case_.k, Ad.data_ptr(), case_.lda, Bd.data_ptr(),
@@ -457,6 +467,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             rr = time_rotating([make(*o) for o in copies], stream, args.rep_ms)
             extras[name].update(hbm_fields(nbytes, t, rr))
             del copies
+        with_traffic(name, traffic)
         extras[name]["clocks"] = line_clocks(t0)
 
     def hbm_fields(nbytes, t_flushed, rot):
@@ -484,7 +495,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         c = clock_log.summary(t0, time.time())
         return {"sm_mhz": c["sm_mhz"], "reasons": c["reasons"], "samples": c["samples"]}
 
-    def tf32x3_line(name, case_):
+    def tf32x3_line(name, case_, traffic=None):
         Ad = torch.from_numpy(case_.A).to(dev)
         Bd = torch.from_numpy(case_.B).to(dev)
         Cd = torch.from_numpy(case_.C_init).to(dev)
@@ -509,8 +520,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                              "three tensor-core products per useful flop",
                         "rep_ms": r["rep_ms"], "calls_per_rep": r["calls_per_rep"],
                         "clocks": line_clocks(t0)}
+        with_traffic(name, traffic)
 
-    def conv_line(name, mode, c, use_ws=False, hbm_bound=False):
+    def conv_line(name, mode, c, use_ws=False, hbm_bound=False, traffic=None):
         OH = om.conv_out_dim(c.H, c.KH, c.stride, c.pad, c.dil)
         OW = om.conv_out_dim(c.W, c.KW, c.stride, c.pad, c.dil)
         L = om.lib()
@@ -545,6 +557,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             rr = time_rotating([make(*o) for o in copies], stream, args.rep_ms)
             extras[name].update(hbm_fields(nbytes, t, rr))
             del copies
+        with_traffic(name, traffic)
         extras[name]["clocks"] = line_clocks(t0)
 
     def chain_line(name, mode):
@@ -568,10 +581,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                         "clocks": line_clocks(t0)}
 
     if not args.headline_only:
-        gemm_line("gemm_4096^3_fast_ws", "fast", case, use_ws=True)
+        SG, CI, CR = "sgemm_tiled_kernel", "conv_implicit_kernel", "conv_rows_kernel"
+        gemm_line("gemm_4096^3_fast_ws", "fast", case, use_ws=True, traffic=(SG, "gemm_4096^3_fast"))
         gemm_line("gemm_4096^3_exact_no_workspace", "exact", case)
         gemm_line("gemm_4096^3_fast_no_workspace", "fast", case)
-        tf32x3_line("gemm_4096^3_tf32x3", case)
+        tf32x3_line("gemm_4096^3_tf32x3", case, traffic=("gemm_tf32x3_kernel", "gemm_4096^3_tf32x3"))
         gemm_line("gemm_prefill_512x11008x4096_exact_ws", "exact",
                   synth.workload_gemm_prefill(False), use_ws=True)
         gemm_line("gemm_prefill_509x11005x4096_exact_ws", "exact",
@@ -579,10 +593,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         gemm_line("gemm_prefill_512x11008x4096_fast_ws", "fast",
                   synth.workload_gemm_prefill(False), use_ws=True)
         gemm_line("gemm_prefill_509x11005x4096_fast_ws", "fast",
-                  synth.workload_gemm_prefill(True), use_ws=True)
+                  synth.workload_gemm_prefill(True), use_ws=True, traffic=(SG, "gemm_prefill_ragged_fast"))
         for md in ("exact", "fast"):
-            conv_line(f"conv3x3_n32_c64_56_{md}_ws", md, synth.workload_conv3x3(), use_ws=True)
-            conv_line(f"conv1x1_n32_c256to64_56_{md}_ws", md, synth.workload_conv1x1(), use_ws=True)
+            conv_line(f"conv3x3_n32_c64_56_{md}_ws", md, synth.workload_conv3x3(), use_ws=True,
+                      traffic=(CR, f"conv3x3_{md}"))
+            conv_line(f"conv1x1_n32_c256to64_56_{md}_ws", md, synth.workload_conv1x1(), use_ws=True,
+                      traffic=(CI, f"conv1x1_{md}"))
         conv_line("conv_g32_s2_d2_n16_c256_28_exact_ws", "exact", synth.workload_conv_grouped(),
                   use_ws=True)
         gemm_line("gemm_prefill_512x11008x4096_exact", "exact", synth.workload_gemm_prefill(False))
@@ -592,13 +608,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         for md in ("exact", "fast"):
             conv_line(f"conv3x3_n32_c64_56_{md}", md, synth.workload_conv3x3())
             conv_line(f"conv1x1_n32_c256to64_56_{md}", md, synth.workload_conv1x1())
-        conv_line("conv_g32_s2_d2_n16_c256_28_exact", "exact", synth.workload_conv_grouped())
+        conv_line("conv_g32_s2_d2_n16_c256_28_exact", "exact", synth.workload_conv_grouped(),
+                  traffic=("conv_group_kernel", "conv_grouped_exact"))
         conv_line("conv_g32_s2_d2_n16_c256_28_fast", "fast", synth.workload_conv_grouped())
         for md in ("exact", "fast"):
             conv_line(f"conv_dw3x3_n32_c256_56_{md}", md, synth.workload_conv_depthwise(),
-                      hbm_bound=True)
+                      hbm_bound=True, traffic=("conv_dw_tma_kernel", f"conv_depthwise_{md}"))
             gemm_line(f"gemm_decode_1x11008x4096_{md}", md, synth.workload_gemm_decode(),
-                      hbm_bound=True)
+                      hbm_bound=True, traffic=("gemv_kernel", f"gemm_decode_{md}"))
         for md in ("exact", "fast"):
             conv_line(f"conv_late3x3_n1_c512_7_{md}", md, synth.workload_conv_late3x3())
         for md in ("exact", "fast"):
