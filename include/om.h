@@ -112,8 +112,8 @@ OM_API int64_t om_conv_out_dim(int64_t size, int64_t ksize, int64_t stride, int6
  * copies for both; products with at most 8 rows or 8 columns run as
  * matrix-vector products. Every path gives identical bits.
  * OM_MODE_TF32X3: each operand is split into a TF32 high part (truncated)
- * and a TF32 low part (the rounded remainder); C accumulates
- * hi*hi + hi*lo + lo*hi in fp32 on the tensor cores.
+ * and a low part (the remainder, of which the tensor cores read the TF32
+ * part); C accumulates hi*hi + hi*lo + lo*hi in fp32 on the tensor cores.
  * Bound, for outputs whose exact-mode result is finite:
  *   |C - C_exact| <= 1e-5 * sqrt(k) * sum_p |A[i][p]| * |B[p][j]|.
  * Non-finite inputs give non-finite outputs where the exact result is

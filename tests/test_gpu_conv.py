@@ -200,6 +200,22 @@ def test_conv3x3_workload_sampled_images(mode, name):
 
 
 @pytest.mark.parametrize("mode,name", MODES)
+def test_depthwise_workload_sampled_images(mode, name):
+    # the benchmark's depthwise line (TMA window ring kernel), first and last image
+    c = synth.workload_conv_depthwise()
+    got = run_conv(c, name)
+    for n0 in (0, 31):
+        assert_bits_equal(got[n0:n0 + 1], want_conv(c, mode, (n0, n0 + 1)), f"depthwise image {n0}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_late3x3_workload_full_size(mode, name):
+    # the benchmark's batch-1 7x7 layer (column kernel), whole output
+    c = synth.workload_conv_late3x3()
+    assert_bits_equal(run_conv(c, name), want_conv(c, mode), "late 3x3 workload")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
 def test_conv1x1_workload_sampled_images(mode, name):
     c = synth.workload_conv1x1()
     got = run_conv(c, name)

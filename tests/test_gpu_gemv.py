@@ -102,6 +102,13 @@ def test_decode_shaped_product(mode, name):
 
 
 @pytest.mark.parametrize("mode,name", MODES)
+def test_decode_workload_full_size(mode, name):
+    # the benchmark's decode line: its own seeded operands, whole output
+    case = synth.workload_gemm_decode()
+    assert_bits_equal(run_gemm(case, name), want_gemm(case, mode), "decode workload")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
 def test_forced_gemv_on_a_wide_product_falls_back(mode, name):
     case = synth.make_gemm("gv", 40, 50, 20, seed=3)
     assert_bits_equal(run_gemm(case, name, cfg=5), want_gemm(case, mode), "forced gemv 40x50")
