@@ -218,10 +218,11 @@ OM_API int om_gemm_f32_no_alloc(int64_t m, int64_t n, int64_t k,
  * group's output planes. Padding is never materialised. Shapes the
  * implicit product would run poorly go to other kernels with the same
  * per-output loop and the same bits: groups of at most 16 output channels
- * (depthwise included) and layers with few output pixels run from input
- * windows staged in on-chip memory (zero border written at copy time), and a
- * 1x1 kernel over a 1x1 input of at most 8 images runs as a matrix-vector
- * product.
+ * (depthwise included), stride-1 3x3 layers whose output-row segments fill
+ * the GPU, and layers with few output pixels run from input windows staged
+ * in on-chip memory (zero border written at copy time; by TMA with its
+ * out-of-range fill where input rows are 16-byte aligned), and a 1x1 kernel
+ * over a 1x1 input of at most 8 images runs as a matrix-vector product.
  *   x: [N][Cin][H][W] contiguous.
  *   w: [Cout][Cin/G][KH][KW] contiguous.
  *   y: [N][Cout][OutH][OutW] contiguous, OutH/OutW from om_conv_out_dim.
