@@ -323,3 +323,46 @@ def test_group_window_kernel_wide_shapes(shape, mode, name, cfg):
     c = synth.make_conv("t", *shape, seed=sum(shape) + 9, dist_x=("uniform", -1, 1),
                         dist_w=("normal", 0, 0.5))
     assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"group window {shape} cfg={cfg}")
+
+
+@pytest.mark.parametrize("mode,name", MODES)
+def test_group_window_kernel_packed_weights_and_unaligned_input(mode, name):
+    # packed weights (rows padded to 4 floats) through the TMA window kernel,
+    # and the same layer with x 4 bytes past a 16-byte boundary (the copy
+    # kernel takes it): identical bits
+    import torch
+    c = synth.make_conv("t", 3, 36, 14, 16, 48, 4, 3, 3, 2, 1, 2, seed=21, dist_x=("uniform", -1, 1),
+                        dist_w=("normal", 0, 0.5))
+    want = want_conv(c, mode)
+    assert_bits_equal(run_conv(c, name, None, packed=True), want, "packed, group window")
+    xbuf = torch.zeros(c.x.size + 4, dtype=torch.float32, device="cuda")
+    xbuf[1:1 + c.x.size] = to_dev(c.x).reshape(-1)
+    x = xbuf[1:1 + c.x.size]
+    assert x.data_ptr() % 16 == 4
+    w = to_dev(c.w)
+    y = torch.empty(want.shape, device="cuda")
+    st = om.lib().om_conv2d_f32(c.N, c.Cin, c.H, c.W, c.Cout, c.G, c.KH, c.KW, c.stride, c.pad, c.dil,
+                                x.data_ptr(), w.data_ptr(), y.data_ptr(), om.MODES[name], None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert_bits_equal(y.cpu().numpy(), want, "misaligned group layer")
+
+
+# The small-group TMA window kernel at its box limits: 256 input channels per
+# group (the box's channel extent), a 256-column box, a band of one row of
+# 248 output pixels, and many bands per plane.
+GROUP_LIMITS = [
+    (1, 512, 6, 8, 16, 2, 1, 1, 1, 0, 1),
+    (1, 8, 5, 252, 8, 2, 1, 1, 1, 0, 1),
+    (2, 16, 3, 248, 16, 4, 3, 3, 1, 1, 1),
+    (1, 8, 300, 12, 8, 2, 3, 3, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("shape", GROUP_LIMITS)
+@pytest.mark.parametrize("mode,name", MODES)
+def test_group_window_kernel_limits(shape, mode, name):
+    c = synth.make_conv("t", *shape, seed=sum(shape) + 31, dist_x=("uniform", -1, 1),
+                        dist_w=("normal", 0, 0.5))
+    for cfg in (7, None):
+        assert_bits_equal(run_conv(c, name, cfg), want_conv(c, mode), f"group limits {shape} cfg={cfg}")
